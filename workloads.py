@@ -1,0 +1,225 @@
+"""Seeded synthetic inputs for paged-KV attention: the one module that both the
+CPU oracle's tests and the GPU path use.
+
+It holds no attention arithmetic: it draws bf16 tensors, lays key/value rows
+out in a paged cache under a seeded random page permutation, and writes the
+CSR arrays (qo_indptr, kv_indptr, kv_indices, kv_last_page_len) that describe
+a call.  Every sequence draws its own values from its own seeds, so a request
+has the same bits whether it runs alone or inside any batch, and whatever
+physical pages it lands on.
+
+Terms: a *sequence* has ``prefix`` cached tokens followed by ``new`` tokens;
+its key/value rows cover prefix+new positions and its queries cover the new
+tokens.  A *call* is a list of parts (sequence, q_start, q_end): the part's
+queries are new tokens q_start..q_end-1 and it sees the first
+prefix+q_end keys.  Decode is a call whose parts each carry one query.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+BF16 = torch.bfloat16
+
+
+@dataclass(frozen=True)
+class Sequence:
+    seed: int
+    prefix: int
+    new: int
+
+    @property
+    def length(self) -> int:
+        return self.prefix + self.new
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def draw_normal_bf16(shape, seed: int, device) -> torch.Tensor:
+    """i.i.d. N(0, 1) values rounded to bf16 (round-to-nearest-even)."""
+    t = torch.randn(shape, generator=_gen(seed, device), device=device, dtype=torch.float32)
+    return t.to(BF16)
+
+
+def uniform_lengths(n: int, lo: int, hi: int, seed: int) -> list[int]:
+    """n integers uniform in [lo, hi]; value i comes from its own seed
+    (seed + i), so the first values do not depend on n."""
+    out = []
+    for i in range(n):
+        g = _gen(seed + i, "cpu")
+        out.append(int(torch.randint(lo, hi + 1, (1,), generator=g).item()))
+    return out
+
+
+@dataclass
+class PagedStore:
+    """Key/value rows of a set of sequences in one paged cache pair.
+
+    k_cache / v_cache: [num_pages, page_size, num_kv_heads, head_dim] bf16.
+    pages[i]: physical page ids of sequence i in order.  Slots past the end of
+    a sequence's last page are filled with NaN so that any read of them shows.
+    """
+    seqs: list
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    device: str
+    layout_seed: int = 7
+    spare_pages: int = 0
+    k_cache: torch.Tensor = field(init=False)
+    v_cache: torch.Tensor = field(init=False)
+    q: list = field(init=False)
+    pages: list = field(init=False)
+
+    def __post_init__(self):
+        P, Hkv, D, Hq = self.page_size, self.num_kv_heads, self.head_dim, self.num_qo_heads
+        counts = [-(-s.length // P) for s in self.seqs]
+        num_pages = sum(counts) + self.spare_pages
+        perm = torch.randperm(max(num_pages, 1), generator=_gen(self.layout_seed, "cpu"))
+        self.k_cache = torch.full((max(num_pages, 1), P, Hkv, D), float("nan"), dtype=BF16,
+                                  device=self.device)
+        self.v_cache = torch.full_like(self.k_cache, float("nan"))
+        self.q, self.pages = [], []
+        start = 0
+        for s, c in zip(self.seqs, counts):
+            ids = perm[start:start + c].to(torch.int32)
+            start += c
+            self.pages.append(ids)
+            base = 4 * int(s.seed)
+            self.q.append(draw_normal_bf16((s.new, Hq, D), base + 1, self.device))
+            if c == 0:
+                continue
+            for cache, sub in ((self.k_cache, 2), (self.v_cache, 3)):
+                rows = draw_normal_bf16((s.length, Hkv, D), base + sub, self.device)
+                padded = torch.full((c * P, Hkv, D), float("nan"), dtype=BF16, device=self.device)
+                padded[: s.length] = rows
+                cache[ids.to(self.device).long()] = padded.view(c, P, Hkv, D)
+
+    @property
+    def num_pages(self) -> int:
+        return self.k_cache.shape[0]
+
+
+@dataclass
+class Call:
+    """One prefill/extend or decode call: what the library entry points take."""
+    store: PagedStore
+    parts: list  # (sequence index, q_start, q_end)
+    q: torch.Tensor
+    qo_indptr: torch.Tensor  # int32, CPU
+    kv_indptr: torch.Tensor  # int32, CPU
+    kv_indices: torch.Tensor  # int32, CPU
+    kv_last_page_len: torch.Tensor  # int32, CPU
+    q_lens: list
+    kv_lens: list
+
+    @property
+    def batch(self) -> int:
+        return len(self.parts)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.qo_indptr[-1])
+
+
+def make_call(store: PagedStore, parts) -> Call:
+    """Assemble the CSR description of a call over ``store``."""
+    P = store.page_size
+    qs, q_lens, kv_lens, idx, last = [], [], [], [], []
+    qo, kvp = [0], [0]
+    for (si, a, b) in parts:
+        s = store.seqs[si]
+        if not (0 <= a <= b <= s.new):
+            raise ValueError(f"part {(si, a, b)} outside sequence of {s.new} new tokens")
+        kv_len = s.prefix + b
+        n_pages = -(-kv_len // P)
+        qs.append(store.q[si][a:b])
+        q_lens.append(b - a)
+        kv_lens.append(kv_len)
+        idx.append(store.pages[si][:n_pages])
+        last.append(kv_len - (n_pages - 1) * P if n_pages > 0 else 0)
+        qo.append(qo[-1] + (b - a))
+        kvp.append(kvp[-1] + n_pages)
+    Hq, D = store.num_qo_heads, store.head_dim
+    q = torch.cat(qs, 0) if qs else torch.zeros((0, Hq, D), dtype=BF16, device=store.device)
+    kv_indices = torch.cat(idx) if idx else torch.zeros(0, dtype=torch.int32)
+    return Call(store, list(parts), q.contiguous(), torch.tensor(qo, dtype=torch.int32),
+                torch.tensor(kvp, dtype=torch.int32), kv_indices.to(torch.int32).cpu(),
+                torch.tensor(last, dtype=torch.int32), q_lens, kv_lens)
+
+
+def whole_prefill(store: PagedStore) -> Call:
+    """Every sequence extended by all its new tokens in one call."""
+    return make_call(store, [(i, 0, s.new) for i, s in enumerate(store.seqs)])
+
+
+def chunked_calls(store: PagedStore, chunk: int) -> list:
+    """Step c extends every sequence by its new tokens [c*chunk, (c+1)*chunk)."""
+    steps = max((-(-s.new // chunk)) for s in store.seqs)
+    calls = []
+    for c in range(steps):
+        parts = []
+        for i, s in enumerate(store.seqs):
+            a = c * chunk
+            if a < s.new:
+                parts.append((i, a, min(s.new, a + chunk)))
+        calls.append(make_call(store, parts))
+    return calls
+
+
+def bf16_bits(t: torch.Tensor):
+    """Raw bf16 bit patterns of a tensor as a CPU numpy uint16 array."""
+    import numpy as np
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# The five workloads (Qwen3-8B shapes: 32 q heads, 8 kv heads, head_dim 128).
+
+QWEN = dict(num_qo_heads=32, num_kv_heads=8, head_dim=128)
+
+
+def cfg1_tiny(device) -> PagedStore:
+    """1 request, q_len = kv_len = 256, 4 q / 1 kv head, head_dim 64, page 16."""
+    return PagedStore([Sequence(1000, 0, 256)], 4, 1, 64, 16, device, layout_seed=1999)
+
+
+def cfg2_prefill(device, batch: int = 8, first: int = 0) -> PagedStore:
+    """Batched prefill: lengths uniform in [512, 8192], page 1.  ``first``
+    selects requests first..first+batch-1 of the same seeded population."""
+    lens = uniform_lengths(first + batch, 512, 8192, 2000)[first:]
+    seqs = [Sequence(2000 + first + i, 0, L) for i, L in enumerate(lens)]
+    return PagedStore(seqs, page_size=1, device=device, layout_seed=2999 + first, **QWEN)
+
+
+def cfg3_prefix(device, new: int = 16384, prefixes=(1, 511, 2048, 4097)) -> PagedStore:
+    """Chunked prefill with cached prefixes 1/511/2048/4097 + 16384 new tokens."""
+    seqs = [Sequence(3000 + i, p, new) for i, p in enumerate(prefixes)]
+    return PagedStore(seqs, page_size=1, device=device, layout_seed=3999, **QWEN)
+
+
+def cfg4_decode(device, batch: int, lo: int = 1024, hi: int = 32768) -> PagedStore:
+    """Decode: contexts uniform in [1024, 32768]; the last context token is the
+    query, so each sequence has ctx-1 cached tokens and 1 new token."""
+    lens = uniform_lengths(batch, lo, hi, 4000)
+    seqs = [Sequence(4000 + i, L - 1, 1) for i, L in enumerate(lens)]
+    return PagedStore(seqs, page_size=1, device=device, layout_seed=4999 + batch, **QWEN)
+
+
+def cfg5_mixed(device, n_extend: int = 64, n_decode: int = 32, decode_ctx: int = 131072,
+               chunk: int = 4096, chunk_prefix: int = 4096):
+    """Mixed serving batch, page 16: one prefill chunk (prefix 4096 + 4096 new),
+    one-token extends (contexts uniform in [1024, 32768]) and decodes at
+    131072 context.  Returns (prefill store, decode store)."""
+    ext = uniform_lengths(n_extend, 1024, 32768, 5100)
+    pre = [Sequence(5000, chunk_prefix, chunk)] + [
+        Sequence(5100 + i, L - 1, 1) for i, L in enumerate(ext)]
+    dec = [Sequence(5500 + i, decode_ctx - 1, 1) for i in range(n_decode)]
+    return (PagedStore(pre, page_size=16, device=device, layout_seed=5999, **QWEN),
+            PagedStore(dec, page_size=16, device=device, layout_seed=5998, **QWEN))
