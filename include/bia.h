@@ -1,0 +1,190 @@
+/*
+ * bia.h - batch-invariant paged-KV grouped-query attention for one GB300
+ * (sm_103a).  C ABI of libbia.so.
+ *
+ * The operation is the paged-KV prefill / decode attention that the pages
+ * describe as FlashInfer's BatchPrefillWithPagedKVCacheWrapper and decode
+ * wrapper run with a fixed split-KV tile ("sglang PR #43612", Summary;
+ * "sglang PR #10417 [POC] Support deterministic inference", Modifications:
+ * paged prefill for every prefill, split-KV fixed to 2048 for decode and
+ * 4096 for prefill).  A request's output bits depend only on its own
+ * q/k/v values and lengths, head_dim, the GQA group size and the split size:
+ * never on the batch it is in, the order of that batch, the physical pages
+ * it occupies, the number of SMs or the launch grid, or where a chunk
+ * boundary falls ("sglang PR #43612", Summary: chunked prefill must
+ * reproduce the unchunked one when chunks start on the 128-row q-tile grid,
+ * 128 / gqa_group tokens; this library also reproduces it off that grid, but
+ * callers may only rely on the grid).
+ *
+ * Layouts (all row-major, all device pointers unless named *_host):
+ *   q        [total_q, num_qo_heads, head_dim] bf16 (decode: [batch, ...])
+ *   k_cache  [num_pages, page_size, num_kv_heads, head_dim] bf16
+ *   v_cache  same as k_cache
+ *   out      [total_q, num_qo_heads, head_dim] bf16
+ *   lse      [total_q, num_qo_heads] fp32, natural log; may be NULL
+ *   qo_indptr [batch+1] int32: request b owns q tokens
+ *            qo_indptr[b] .. qo_indptr[b+1]-1 (qo_indptr[0] == 0)
+ *   kv_indptr [batch+1] int32: request b owns pages
+ *            kv_indices[kv_indptr[b] .. kv_indptr[b+1]-1], in key order
+ *   kv_last_page_len [batch] int32 in 1..page_size (ignored for a request
+ *            that owns no page)
+ * Request b has kv_len = (n_pages-1)*page_size + kv_last_page_len[b] keys;
+ * key j sits at page kv_indices[kv_indptr[b] + j/page_size], slot
+ * j % page_size.  Its q tokens are the LAST q_len positions of the sequence:
+ * in-call token t is at absolute position kv_len - q_len + t, and a causal
+ * row sees keys 0..that position.  q head h reads kv head
+ * h / (num_qo_heads / num_kv_heads).  sm_scale <= 0 selects 1/sqrt(head_dim).
+ *
+ * Ownership: the caller owns every buffer and the stream; the library never
+ * allocates device memory and never synchronises the stream.  The *_host
+ * arrays are read synchronously during the call (to validate and to size the
+ * launch) and must equal their device copies.  All work is enqueued on
+ * `stream` (a cudaStream_t; NULL = legacy default stream).
+ *
+ * Errors: every entry point returns BIA_OK or a negative bia_status and never
+ * aborts.  Host-side checks run before anything is enqueued.  A page index
+ * outside [0, num_pages) is caught on the device: the row is read as zeros and
+ * bit 0 of the workspace status word is set (bia_read_status).
+ *
+ * Supported: head_dim 64 or 128; num_qo_heads / num_kv_heads in {1,2,4,8};
+ * page_size a power of two in 1..256; split sizes positive multiples of 128.
+ */
+#ifndef BIA_H
+#define BIA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BIA_API __attribute__((visibility("default")))
+#else
+#define BIA_API
+#endif
+
+/* Rows of one prefill q tile: (token, q head of the group) pairs, GQA-packed
+ * ("sglang PR #43612", Summary: the 128-row q-tile grid). */
+#define BIA_Q_TILE_ROWS 128
+/* Default fixed split-KV sizes ("sglang PR #10417", Modifications). */
+#define BIA_PREFILL_SPLIT 4096
+#define BIA_DECODE_SPLIT 2048
+
+typedef enum bia_status {
+    BIA_OK = 0,
+    BIA_ERR_INVALID_ARG = -1,         /* null pointer, bad indptr, q_len > kv_len (causal) ... */
+    BIA_ERR_UNSUPPORTED = -2,         /* head_dim, GQA group, page size or split not supported */
+    BIA_ERR_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes below the *_workspace_size answer */
+    BIA_ERR_CUDA = -4                 /* a CUDA call or launch failed */
+} bia_status;
+
+typedef struct bia_attn_desc {
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;  /* 64 or 128 */
+    int32_t page_size; /* power of two, 1..256 */
+    float sm_scale;    /* <= 0: 1/sqrt(head_dim) */
+} bia_attn_desc;
+
+/*
+ * Causal (or full) prefill / chunked-prefill extend of a batch of requests
+ * against the paged KV cache.  Rows are processed in 128-row q tiles
+ * (128/G tokens x G heads of one kv head), keys in 128-key blocks anchored at
+ * absolute key 0, and each row's keys in fixed split-KV tiles of split_size
+ * keys (also anchored at key 0); a row's split partials are merged in
+ * ascending split order by log-sum-exp ("sglang PR #10417", Modifications;
+ * "sglang PR #43612", Summary).
+ *   causal:     1 = causal extend, 0 = every row sees all kv_len keys
+ *   split_size: keys per split-KV tile, multiple of 128; 0 = BIA_PREFILL_SPLIT
+ *   workspace:  >= bia_prefill_workspace_size(...) bytes, 256-byte aligned;
+ *               its contents on entry do not matter
+ *   out / lse:  written for every q row (lse may be NULL)
+ */
+BIA_API int bia_prefill_paged(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                      const void *v_cache, int64_t num_pages, const int32_t *qo_indptr,
+                      const int32_t *kv_indptr, const int32_t *kv_indices,
+                      const int32_t *kv_last_page_len, const int32_t *qo_indptr_host,
+                      const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                      int32_t batch, int32_t causal, int32_t split_size, void *workspace,
+                      size_t workspace_bytes, void *out, float *lse, void *stream);
+
+/* Workspace bytes bia_prefill_paged needs for this call (0 on invalid input). */
+BIA_API size_t bia_prefill_workspace_size(const bia_attn_desc *desc, const int32_t *qo_indptr_host,
+                                  const int32_t *kv_indptr_host,
+                                  const int32_t *kv_last_page_len_host, int32_t batch,
+                                  int32_t causal, int32_t split_size);
+
+/*
+ * Decode: one query token per request (q [batch, Hq, D]) against its whole
+ * paged context, in fixed split-KV tiles of split_size keys (0 =
+ * BIA_DECODE_SPLIT) whose partials are merged in ascending order
+ * ("sglang PR #10417", Modifications: split-KV fixed to 2048 for decode).
+ * Every request must own at least one key.
+ */
+BIA_API int bia_decode_paged(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                     const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
+                     const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                     const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                     int32_t batch, int32_t split_size, void *workspace, size_t workspace_bytes,
+                     void *out, float *lse, void *stream);
+
+/* Workspace bytes bia_decode_paged needs for this call (0 on invalid input). */
+BIA_API size_t bia_decode_workspace_size(const bia_attn_desc *desc, const int32_t *kv_indptr_host,
+                                 const int32_t *kv_last_page_len_host, int32_t batch,
+                                 int32_t split_size);
+
+/*
+ * Fixed-order log-sum-exp merge of attention states (the merge the split-KV
+ * partials of "sglang PR #10417", Modifications, need; the pages fix only
+ * that its order is fixed).  For row (i, h) the states s = 0..count-1 are
+ * folded left to right:
+ *   M = max(L, lse_s); a = e^{L-M}; b = e^{lse_s-M};
+ *   o = (a*o + b*v_s) / (a+b); L = M + ln(a+b)
+ * starting from the first state; a state with lse = -inf is skipped, and a
+ * row with no finite state yields out 0 and lse -inf.
+ *   v:          [n, num_states_max, num_heads, head_dim] fp32
+ *   s:          [n, num_states_max, num_heads] fp32, natural-log LSE
+ *   num_states: [n] int32 device array of counts <= num_states_max, or NULL
+ *   out:        [n, num_heads, head_dim] bf16 (round to nearest even)
+ *   out_lse:    [n, num_heads] fp32 or NULL
+ * head_dim: a multiple of 4 up to 512.
+ */
+BIA_API int bia_merge_states(const float *v, const float *s, const int32_t *num_states, int64_t n,
+                     int32_t num_states_max, int32_t num_heads, int32_t head_dim, void *out,
+                     float *out_lse, void *stream);
+
+/* Tokens per q tile for GQA group size G = num_qo_heads / num_kv_heads:
+ * 128 / G, the chunk grid on which chunked prefill is guaranteed to be
+ * bit-identical ("sglang PR #43612", Summary).  0 if G does not divide 128. */
+BIA_API int32_t bia_q_tile_tokens(int32_t gqa_group);
+
+/* Static text for a bia_status value. */
+BIA_API const char *bia_status_string(int status);
+
+/*
+ * Copies the device status word of the last call that used `workspace`
+ * (bit 0: a page index was out of range; bit 1: the device plan disagreed with
+ * the host-sized launch; bit 2: a device wait timed out) into *status_out.
+ * Synchronises `stream`.
+ */
+BIA_API int bia_read_status(const void *workspace, int32_t *status_out, void *stream);
+
+/*
+ * Measurement hooks (not part of the computation).
+ * bia_set_profile_events: when both are non-NULL, every later prefill /
+ * decode call records `attn_begin` just before and `attn_end` just after its
+ * attention kernel on the call's stream (cudaEvent_t handles owned by the
+ * caller), so the kernel alone can be timed; NULL, NULL turns this off.
+ * Process-wide, not thread-safe.
+ * bia_launch_count: kernels this library has launched since it was loaded.
+ */
+BIA_API void bia_set_profile_events(void *attn_begin, void *attn_end);
+BIA_API uint64_t bia_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIA_H */

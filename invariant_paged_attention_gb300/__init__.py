@@ -1,0 +1,188 @@
+"""Python binding of libbia.so: batch-invariant paged-KV GQA attention on
+GB300 (sm_103a).
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of libbia.so; PyTorch supplies device memory and streams.  There is
+no fallback: if the library is missing or fails to load, every call raises.
+
+The functions carry the C names of ``include/bia.h`` and take torch tensors:
+device tensors for the data and the device copies of the index arrays, CPU
+int32 tensors for the host mirrors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbia.so")
+
+BIA_OK = 0
+BIA_ERR_INVALID_ARG = -1
+BIA_ERR_UNSUPPORTED = -2
+BIA_ERR_WORKSPACE_TOO_SMALL = -3
+BIA_ERR_CUDA = -4
+BIA_Q_TILE_ROWS = 128
+BIA_PREFILL_SPLIT = 4096
+BIA_DECODE_SPLIT = 2048
+
+# every symbol include/bia.h exports
+EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged",
+           "bia_decode_workspace_size", "bia_merge_states", "bia_q_tile_tokens",
+           "bia_status_string", "bia_read_status", "bia_set_profile_events",
+           "bia_launch_count")
+
+
+class BiaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where} failed: {status_string(status)} ({status})")
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("num_qo_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Loads libbia.so (built by ``build.build()``); raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libbia.so not built at {path}: run "
+                           "`python -m invariant_paged_attention_gb300.build`")
+    lib = ctypes.CDLL(path)
+    i32, i64, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    dp = ctypes.POINTER(AttnDesc)
+    lib.bia_prefill_paged.argtypes = [dp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                      i32, vp, sz, vp, vp, vp]
+    lib.bia_prefill_paged.restype = ctypes.c_int
+    lib.bia_prefill_workspace_size.argtypes = [dp, vp, vp, vp, i32, i32, i32]
+    lib.bia_prefill_workspace_size.restype = sz
+    lib.bia_decode_paged.argtypes = [dp, vp, vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, vp, sz,
+                                     vp, vp, vp]
+    lib.bia_decode_paged.restype = ctypes.c_int
+    lib.bia_decode_workspace_size.argtypes = [dp, vp, vp, i32, i32]
+    lib.bia_decode_workspace_size.restype = sz
+    lib.bia_merge_states.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp, vp, vp]
+    lib.bia_merge_states.restype = ctypes.c_int
+    lib.bia_q_tile_tokens.argtypes = [i32]
+    lib.bia_q_tile_tokens.restype = i32
+    lib.bia_status_string.argtypes = [ctypes.c_int]
+    lib.bia_status_string.restype = ctypes.c_char_p
+    lib.bia_read_status.argtypes = [vp, ctypes.POINTER(i32), vp]
+    lib.bia_read_status.restype = ctypes.c_int
+    lib.bia_set_profile_events.argtypes = [vp, vp]
+    lib.bia_set_profile_events.restype = None
+    lib.bia_launch_count.argtypes = []
+    lib.bia_launch_count.restype = ctypes.c_uint64
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_i32(t) -> torch.Tensor:
+    t = torch.as_tensor(t, dtype=torch.int32)
+    if t.device.type != "cpu":
+        raise ValueError("host mirrors must be CPU tensors")
+    return t.contiguous()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_desc(num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale=0.0) -> AttnDesc:
+    return AttnDesc(num_qo_heads, num_kv_heads, head_dim, page_size, float(sm_scale))
+
+
+def status_string(status: int) -> str:
+    return load().bia_status_string(int(status)).decode()
+
+
+def bia_q_tile_tokens(gqa_group: int) -> int:
+    return int(load().bia_q_tile_tokens(int(gqa_group)))
+
+
+def bia_prefill_workspace_size(desc, qo_indptr_host, kv_indptr_host, kv_last_page_len_host,
+                               causal=True, split_size=0) -> int:
+    qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
+                     _host_i32(kv_last_page_len_host))
+    return int(load().bia_prefill_workspace_size(ctypes.byref(desc), _ptr(qo), _ptr(kvp),
+                                                 _ptr(last), len(qo) - 1, int(bool(causal)),
+                                                 int(split_size)))
+
+
+def bia_decode_workspace_size(desc, kv_indptr_host, kv_last_page_len_host, split_size=0) -> int:
+    kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
+    return int(load().bia_decode_workspace_size(ctypes.byref(desc), _ptr(kvp), _ptr(last),
+                                                len(kvp) - 1, int(split_size)))
+
+
+def bia_prefill_paged(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices,
+                      kv_last_page_len, qo_indptr_host, kv_indptr_host, kv_last_page_len_host,
+                      workspace, out, lse=None, causal=True, split_size=0, stream=None):
+    qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
+                     _host_i32(kv_last_page_len_host))
+    rc = load().bia_prefill_paged(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(qo),
+        _ptr(kvp), _ptr(last), len(qo) - 1, int(bool(causal)), int(split_size), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_prefill_paged")
+
+
+def bia_decode_paged(desc, q, k_cache, v_cache, kv_indptr, kv_indices, kv_last_page_len,
+                     kv_indptr_host, kv_last_page_len_host, workspace, out, lse=None,
+                     split_size=0, stream=None):
+    kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
+    rc = load().bia_decode_paged(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(kvp), _ptr(last),
+        len(kvp) - 1, int(split_size), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_decode_paged")
+
+
+def bia_merge_states(v, s, out, out_lse=None, num_states=None, stream=None):
+    """v [n, S, H, D] fp32, s [n, S, H] fp32 -> out [n, H, D] bf16, out_lse [n, H]."""
+    n, S, H, D = v.shape
+    rc = load().bia_merge_states(_ptr(v), _ptr(s), _ptr(num_states), n, S, H, D, _ptr(out),
+                                 _ptr(out_lse), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_merge_states")
+
+
+def bia_read_status(workspace, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    rc = load().bia_read_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_read_status")
+    return int(st.value)
+
+
+def bia_set_profile_events(begin=None, end=None):
+    """Record torch.cuda.Event `begin` / `end` around the attention kernel of
+    every later prefill / decode call (None, None: off)."""
+    h = (lambda e: None if e is None else ctypes.c_void_p(e.cuda_event))
+    load().bia_set_profile_events(h(begin), h(end))
+
+
+def bia_launch_count() -> int:
+    return int(load().bia_launch_count())

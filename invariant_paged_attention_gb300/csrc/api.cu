@@ -1,0 +1,288 @@
+// Host side of libbia.so: argument validation, workspace sizing and the
+// launch sequence (device plan -> attention kernel -> merge of split
+// partials) for each entry point of bia.h.  No allocation, no stream
+// synchronisation (except bia_read_status, which exists to synchronise).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/bia.h"
+#include "bia_internal.h"
+
+namespace {
+
+cudaEvent_t g_attn_begin = nullptr, g_attn_end = nullptr;
+unsigned long long g_launches = 0;
+
+using bia::PlanArgs;
+using bia::AttnArgs;
+using bia::WsLayout;
+
+struct HostPlan {
+  int64_t n_units = 0;
+  int64_t part_rows = 0;
+  int64_t total_q = 0;
+};
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int log2i(int x) {
+  int s = 0;
+  while ((1 << s) < x) ++s;
+  return s;
+}
+
+int check_desc(const bia_attn_desc *d) {
+  if (!d) return BIA_ERR_INVALID_ARG;
+  if (d->num_qo_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->page_size <= 0)
+    return BIA_ERR_INVALID_ARG;
+  if (d->num_qo_heads % d->num_kv_heads != 0) return BIA_ERR_UNSUPPORTED;
+  const int G = d->num_qo_heads / d->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return BIA_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return BIA_ERR_UNSUPPORTED;
+  if (!is_pow2(d->page_size) || d->page_size > 256) return BIA_ERR_UNSUPPORTED;
+  if (!(std::isfinite(d->sm_scale))) return BIA_ERR_INVALID_ARG;
+  return BIA_OK;
+}
+
+// Validates the host mirrors and computes the same plan sizes the device
+// planner will produce.  qo == nullptr: decode (one query per request).
+int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
+              const int32_t *last, int32_t batch, int32_t causal, int32_t split, int tile_tokens,
+              HostPlan *hp) {
+  if (batch <= 0 || !kvp || !last) return BIA_ERR_INVALID_ARG;
+  if (split <= 0 || split % bia::kKvBlock != 0) return BIA_ERR_UNSUPPORTED;
+  if (qo && qo[0] != 0) return BIA_ERR_INVALID_ARG;
+  if (kvp[0] < 0) return BIA_ERR_INVALID_ARG;
+  HostPlan p;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t q_len = qo ? static_cast<int64_t>(qo[b + 1]) - qo[b] : 1;
+    const int64_t pages = static_cast<int64_t>(kvp[b + 1]) - kvp[b];
+    if (q_len < 0 || pages < 0) return BIA_ERR_INVALID_ARG;
+    if (pages > 0 && (last[b] < 1 || last[b] > d->page_size)) return BIA_ERR_INVALID_ARG;
+    const int64_t kv_len = pages > 0 ? (pages - 1) * d->page_size + last[b] : 0;
+    if (kv_len > INT32_MAX / 2) return BIA_ERR_UNSUPPORTED;
+    if (causal && q_len > kv_len) return BIA_ERR_INVALID_ARG;
+    if (!qo && kv_len == 0) return BIA_ERR_INVALID_ARG;
+    const int32_t tiles = static_cast<int32_t>((q_len + tile_tokens - 1) / tile_tokens);
+    int32_t nsp = 1;
+    for (int32_t t = 0; t < tiles; ++t) {
+      const int32_t n = bia::tile_splits(static_cast<int32_t>(q_len), static_cast<int32_t>(kv_len),
+                                         t, tile_tokens, causal, split);
+      p.n_units += n;
+      if (n > nsp) nsp = n;
+    }
+    if (nsp > 1) p.part_rows += q_len * nsp;
+    p.total_q += q_len;
+  }
+  if (p.n_units > INT32_MAX) return BIA_ERR_UNSUPPORTED; // grid.x limit is 2^31-1
+  *hp = p;
+  return BIA_OK;
+}
+
+float effective_scale(const bia_attn_desc *d) {
+  const float s = d->sm_scale > 0.f ? d->sm_scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
+  return s * 1.4426950408889634f;
+}
+
+int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const void *k_cache,
+                  const void *v_cache, int64_t num_pages, const int32_t *qo_indptr,
+                  const int32_t *kv_indptr, const int32_t *kv_indices,
+                  const int32_t *kv_last_page_len, const int32_t *qo_host,
+                  const int32_t *kvp_host, const int32_t *last_host, int32_t batch,
+                  int32_t causal, int32_t split, void *workspace, size_t workspace_bytes,
+                  void *out, float *lse, void *stream) {
+  int rc = check_desc(desc);
+  if (rc != BIA_OK) return rc;
+  if (!q || !k_cache || !v_cache || !kv_indptr || !kv_indices || !kv_last_page_len || !out ||
+      !workspace || num_pages <= 0)
+    return BIA_ERR_INVALID_ARG;
+  if (!decode && (!qo_indptr || !qo_host)) return BIA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BIA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(k_cache) & 15u) ||
+      (reinterpret_cast<uintptr_t>(v_cache) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u))
+    return BIA_ERR_INVALID_ARG;
+  if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
+  const int G = desc->num_qo_heads / desc->num_kv_heads;
+  const int tile_tokens = decode ? 1 : bia::kTileRows / G;
+  if (decode) causal = 1;
+  HostPlan hp;
+  rc = host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal, split,
+                 tile_tokens, &hp);
+  if (rc != BIA_OK) return rc;
+  const WsLayout w = bia::make_layout(batch, hp.n_units, hp.part_rows, desc->num_qo_heads,
+                                      desc->head_dim);
+  if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
+  if (hp.total_q == 0) return BIA_OK;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  PlanArgs pa{};
+  pa.qo_indptr = decode ? nullptr : qo_indptr;
+  pa.kv_indptr = kv_indptr;
+  pa.kv_last_page_len = kv_last_page_len;
+  pa.batch = batch;
+  pa.page_size = desc->page_size;
+  pa.tile_tokens = tile_tokens;
+  pa.causal = causal;
+  pa.split = split;
+  pa.n_units_expected = hp.n_units;
+  pa.part_rows_expected = hp.part_rows;
+  pa.status = reinterpret_cast<int32_t *>(ws + w.status);
+  pa.reqs = reinterpret_cast<bia::ReqInfo *>(ws + w.reqs);
+  pa.units = reinterpret_cast<bia::Unit *>(ws + w.units);
+  if (bia::launch_plan(pa, st) != cudaSuccess) return BIA_ERR_CUDA;
+  __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t *>(q);
+  a.k_cache = static_cast<const uint16_t *>(k_cache);
+  a.v_cache = static_cast<const uint16_t *>(v_cache);
+  a.kv_indices = kv_indices;
+  a.qo_indptr = decode ? nullptr : qo_indptr;
+  a.num_pages = num_pages;
+  a.Hq = desc->num_qo_heads;
+  a.Hkv = desc->num_kv_heads;
+  a.D = desc->head_dim;
+  a.G = G;
+  a.page_shift = log2i(desc->page_size);
+  a.causal = causal;
+  a.split = split;
+  a.tile_tokens = tile_tokens;
+  a.scale_log2 = effective_scale(desc);
+  a.batch = batch;
+  a.n_units = hp.n_units;
+  a.reqs = pa.reqs;
+  a.units = pa.units;
+  a.part_o = reinterpret_cast<float *>(ws + w.part_o);
+  a.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
+  a.total_rows = hp.total_q;
+  a.out = static_cast<uint16_t *>(out);
+  a.lse = lse;
+  a.status = pa.status;
+
+  const bool profile = g_attn_begin != nullptr && g_attn_end != nullptr;
+  if (profile && cudaEventRecord(g_attn_begin, st) != cudaSuccess) return BIA_ERR_CUDA;
+  cudaError_t e = decode ? bia::launch_decode(a, st) : bia::launch_prefill(a, st);
+  if (e != cudaSuccess) return BIA_ERR_CUDA;
+  if (hp.n_units > 0) __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  if (profile && cudaEventRecord(g_attn_end, st) != cudaSuccess) return BIA_ERR_CUDA;
+  if (hp.part_rows > 0) {
+    e = bia::launch_merge_partials(a, st);
+    if (e != cudaSuccess) return BIA_ERR_CUDA;
+    __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  }
+  return BIA_OK;
+}
+
+size_t workspace_size(bool decode, const bia_attn_desc *desc, const int32_t *qo_host,
+                      const int32_t *kvp_host, const int32_t *last_host, int32_t batch,
+                      int32_t causal, int32_t split) {
+  if (check_desc(desc) != BIA_OK) return 0;
+  if (!decode && !qo_host) return 0;
+  if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
+  const int G = desc->num_qo_heads / desc->num_kv_heads;
+  const int tile_tokens = decode ? 1 : bia::kTileRows / G;
+  HostPlan hp;
+  if (host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, decode ? 1 : causal,
+                split, tile_tokens, &hp) != BIA_OK)
+    return 0;
+  return bia::make_layout(batch, hp.n_units, hp.part_rows, desc->num_qo_heads, desc->head_dim)
+      .total;
+}
+
+} // namespace
+
+extern "C" {
+
+int bia_prefill_paged(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                      const void *v_cache, int64_t num_pages, const int32_t *qo_indptr,
+                      const int32_t *kv_indptr, const int32_t *kv_indices,
+                      const int32_t *kv_last_page_len, const int32_t *qo_indptr_host,
+                      const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                      int32_t batch, int32_t causal, int32_t split_size, void *workspace,
+                      size_t workspace_bytes, void *out, float *lse, void *stream) {
+  return run_attention(false, desc, q, k_cache, v_cache, num_pages, qo_indptr, kv_indptr,
+                       kv_indices, kv_last_page_len, qo_indptr_host, kv_indptr_host,
+                       kv_last_page_len_host, batch, causal ? 1 : 0, split_size, workspace,
+                       workspace_bytes, out, lse, stream);
+}
+
+size_t bia_prefill_workspace_size(const bia_attn_desc *desc, const int32_t *qo_indptr_host,
+                                  const int32_t *kv_indptr_host,
+                                  const int32_t *kv_last_page_len_host, int32_t batch,
+                                  int32_t causal, int32_t split_size) {
+  return workspace_size(false, desc, qo_indptr_host, kv_indptr_host, kv_last_page_len_host,
+                        batch, causal ? 1 : 0, split_size);
+}
+
+int bia_decode_paged(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                     const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
+                     const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                     const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                     int32_t batch, int32_t split_size, void *workspace, size_t workspace_bytes,
+                     void *out, float *lse, void *stream) {
+  return run_attention(true, desc, q, k_cache, v_cache, num_pages, nullptr, kv_indptr,
+                       kv_indices, kv_last_page_len, nullptr, kv_indptr_host,
+                       kv_last_page_len_host, batch, 1, split_size, workspace, workspace_bytes,
+                       out, lse, stream);
+}
+
+size_t bia_decode_workspace_size(const bia_attn_desc *desc, const int32_t *kv_indptr_host,
+                                 const int32_t *kv_last_page_len_host, int32_t batch,
+                                 int32_t split_size) {
+  return workspace_size(true, desc, nullptr, kv_indptr_host, kv_last_page_len_host, batch, 1,
+                        split_size);
+}
+
+int bia_merge_states(const float *v, const float *s, const int32_t *num_states, int64_t n,
+                     int32_t num_states_max, int32_t num_heads, int32_t head_dim, void *out,
+                     float *out_lse, void *stream) {
+  if (n < 0 || num_states_max <= 0 || num_heads <= 0 || head_dim <= 0) return BIA_ERR_INVALID_ARG;
+  if (head_dim % 4 != 0 || head_dim > 512) return BIA_ERR_UNSUPPORTED;
+  if (n == 0) return BIA_OK;
+  if (!v || !s || !out) return BIA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(v) & 15u) || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return BIA_ERR_INVALID_ARG;
+  cudaError_t e = bia::launch_merge_states(v, s, num_states, n, num_states_max, num_heads,
+                                           head_dim, static_cast<uint16_t *>(out), out_lse,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return BIA_ERR_CUDA;
+  __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  return BIA_OK;
+}
+
+int32_t bia_q_tile_tokens(int32_t gqa_group) {
+  if (gqa_group <= 0 || bia::kTileRows % gqa_group != 0) return 0;
+  return bia::kTileRows / gqa_group;
+}
+
+const char *bia_status_string(int status) {
+  switch (status) {
+  case BIA_OK: return "ok";
+  case BIA_ERR_INVALID_ARG: return "invalid argument";
+  case BIA_ERR_UNSUPPORTED: return "unsupported configuration";
+  case BIA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+  case BIA_ERR_CUDA: return "CUDA error";
+  default: return "unknown status";
+  }
+}
+
+int bia_read_status(const void *workspace, int32_t *status_out, void *stream) {
+  if (!workspace || !status_out) return BIA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(status_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return BIA_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? BIA_OK : BIA_ERR_CUDA;
+}
+
+void bia_set_profile_events(void *attn_begin, void *attn_end) {
+  g_attn_begin = static_cast<cudaEvent_t>(attn_begin);
+  g_attn_end = static_cast<cudaEvent_t>(attn_end);
+}
+
+uint64_t bia_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+} // extern "C"

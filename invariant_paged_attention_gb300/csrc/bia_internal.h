@@ -1,0 +1,117 @@
+// Internal declarations shared by the host entry points and the kernels of
+// libbia.so: the workspace layout, the device plan records and the kernel
+// launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace bia {
+
+// Status bits in the workspace status word.
+constexpr int32_t kStatusBadPage = 1;     // a page index outside [0, num_pages)
+constexpr int32_t kStatusPlanMismatch = 2; // device plan disagreed with the host-sized launch
+constexpr int32_t kStatusTimeout = 4;      // a bounded device wait gave up
+
+constexpr int kTileRows = 128; // q tile rows (GQA-packed)
+constexpr int kKvBlock = 128;  // keys per block of the prefill inner loop
+
+// Per-request record written by the plan kernel.
+struct ReqInfo {
+  int32_t q_start;  // first global q token
+  int32_t q_len;    // q tokens in this call
+  int32_t kv_len;   // keys
+  int32_t nsp;      // split-KV tiles of the request's last q tile (max over tiles)
+  int64_t rowbase;  // first partial row (rows of [Hq, D] fp32), -1 if none
+  int32_t page_base;// kv_indptr[b]
+  int32_t pad;
+};
+static_assert(sizeof(ReqInfo) == 32, "ReqInfo layout");
+
+// One unit of work: (request, q tile, split) for one kv head (grid.y).
+struct Unit {
+  int32_t b, tile, split, n_splits; // n_splits: split-KV tiles of this q tile
+};
+
+// Byte offsets inside the caller's workspace.
+struct WsLayout {
+  size_t status = 0;   // int32[64]
+  size_t reqs = 0;     // ReqInfo[batch]
+  size_t units = 0;    // Unit[n_units]
+  size_t part_o = 0;   // float[part_rows * Hq * D]
+  size_t part_lse = 0; // float[part_rows * Hq]
+  size_t total = 0;
+};
+
+// Last absolute key position any row of q tile `tile` may see (-1: none).
+// Rows of a tile are its tile_tokens consecutive in-call tokens; token t sits
+// at position kv_len - q_len + t.
+__host__ __device__ inline int32_t tile_last_key(int32_t q_len, int32_t kv_len, int32_t tile,
+                                                 int32_t tile_tokens, int32_t causal) {
+  if (!causal) return kv_len - 1;
+  int32_t last_t = (tile + 1) * tile_tokens;
+  if (last_t > q_len) last_t = q_len;
+  return kv_len - q_len + last_t - 1;
+}
+// Split-KV tiles (anchored at key 0) a q tile touches; at least 1.
+__host__ __device__ inline int32_t tile_splits(int32_t q_len, int32_t kv_len, int32_t tile,
+                                               int32_t tile_tokens, int32_t causal,
+                                               int32_t split) {
+  int32_t last = tile_last_key(q_len, kv_len, tile, tile_tokens, causal);
+  return last < 0 ? 1 : last / split + 1;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout make_layout(int batch, int64_t n_units, int64_t part_rows, int Hq, int D) {
+  WsLayout w;
+  w.status = 0;
+  w.reqs = 256;
+  w.units = align_up(w.reqs + sizeof(ReqInfo) * (size_t)batch, 256);
+  w.part_o = align_up(w.units + sizeof(Unit) * (size_t)n_units, 256);
+  w.part_lse = align_up(w.part_o + sizeof(float) * (size_t)part_rows * Hq * D, 256);
+  w.total = align_up(w.part_lse + sizeof(float) * (size_t)part_rows * Hq, 256);
+  return w;
+}
+
+struct PlanArgs {
+  const int32_t *qo_indptr;  // NULL for decode (one token per request)
+  const int32_t *kv_indptr;
+  const int32_t *kv_last_page_len;
+  int32_t batch, page_size, tile_tokens, causal, split;
+  int64_t n_units_expected, part_rows_expected;
+  int32_t *status;
+  ReqInfo *reqs;
+  Unit *units;
+};
+
+// Geometry of a call shared by the attention kernels.
+struct AttnArgs {
+  const uint16_t *q, *k_cache, *v_cache;
+  const int32_t *kv_indices;
+  const int32_t *qo_indptr; // NULL for decode
+  int64_t num_pages;
+  int32_t Hq, Hkv, D, G, page_shift, causal, split, tile_tokens;
+  float scale_log2; // sm_scale * log2(e)
+  int32_t batch;
+  int64_t n_units;
+  const ReqInfo *reqs;
+  const Unit *units;
+  float *part_o, *part_lse;
+  int64_t total_rows; // total q tokens
+  uint16_t *out;
+  float *lse;
+  int32_t *status;
+};
+
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
+cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_merge_states(const float *v, const float *s, const int32_t *num_states,
+                                int64_t n, int32_t S, int32_t H, int32_t D, uint16_t *out,
+                                float *out_lse, cudaStream_t st);
+
+} // namespace bia

@@ -1,0 +1,150 @@
+"""The C ABI on the host: the library builds for sm_103a, loads, exports every
+symbol bia.h declares, and rejects bad arguments before enqueuing any work
+(so these calls are safe without a GPU: fake, never-dereferenced device
+pointers are passed)."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bia.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def bia():
+    from invariant_paged_attention_gb300 import build
+    build.build()
+    import invariant_paged_attention_gb300 as m
+    m.load()
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"BIA_API[^;(]*?\b(bia_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for name in ("bia_prefill_paged", "bia_decode_paged", "bia_merge_states"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(bia):
+    lib = bia.load()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert sorted(bia.EXPORTS) == declared_symbols()
+    nm = shutil.which("nm")
+    if nm:
+        out = subprocess.run([nm, "-D", "--defined-only", bia.LIB_PATH], capture_output=True,
+                             text=True).stdout
+        exported = set(re.findall(r"\b(bia_\w+)\b", out))
+        assert exported == set(declared_symbols())
+
+
+def test_q_tile_grid(bia):
+    assert bia.bia_q_tile_tokens(4) == 32
+    assert bia.bia_q_tile_tokens(1) == 128
+    assert bia.bia_q_tile_tokens(8) == 16
+    assert bia.bia_q_tile_tokens(3) == 0
+    assert bia.bia_q_tile_tokens(0) == 0
+
+
+def test_status_strings(bia):
+    assert bia.status_string(0) == "ok"
+    assert "workspace" in bia.status_string(-3)
+    assert bia.status_string(12345) == "unknown status"
+
+
+QWEN = dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=1)
+
+
+def test_workspace_size_counts_split_partials(bia):
+    desc = bia.make_desc(**QWEN)
+    qo = torch.tensor([0, 5000], dtype=torch.int32)
+    kvp = torch.tensor([0, 5000], dtype=torch.int32)
+    last = torch.tensor([1], dtype=torch.int32)
+    one_split = bia.bia_prefill_workspace_size(desc, qo, kvp, last, True, 8192)
+    two_splits = bia.bia_prefill_workspace_size(desc, qo, kvp, last, True, 4096)
+    assert one_split > 0
+    # rows that need a merge: all 5000 tokens x 2 splits x 32 heads x (128+1) fp32
+    assert two_splits - one_split >= 5000 * 2 * 32 * 129 * 4
+    # bad inputs answer 0
+    assert bia.bia_prefill_workspace_size(desc, qo, kvp, last, True, 100) == 0
+    assert bia.bia_prefill_workspace_size(bia.make_desc(32, 8, 96, 1), qo, kvp, last) == 0
+    assert bia.bia_decode_workspace_size(desc, kvp, last) > 0
+
+
+FAKE = 1 << 20  # a 256-byte aligned address that is never dereferenced
+
+
+def call_prefill(bia, desc, qo, kvp, last, *, causal=1, split=0, ws_bytes=1 << 30, ws=FAKE,
+                 num_pages=1 << 20):
+    lib = bia.load()
+    qo = torch.tensor(qo, dtype=torch.int32)
+    kvp = torch.tensor(kvp, dtype=torch.int32)
+    last = torch.tensor(last, dtype=torch.int32)
+    p = ctypes.c_void_p
+    return lib.bia_prefill_paged(ctypes.byref(desc), p(FAKE), p(FAKE), p(FAKE), num_pages,
+                                 p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(qo.data_ptr()),
+                                 p(kvp.data_ptr()), p(last.data_ptr()), len(qo) - 1, causal,
+                                 split, p(ws), ws_bytes, p(FAKE), None, None)
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(bia):
+    d = bia.make_desc(**QWEN)
+    inv, uns, small = bia.BIA_ERR_INVALID_ARG, bia.BIA_ERR_UNSUPPORTED, bia.BIA_ERR_WORKSPACE_TOO_SMALL
+    assert call_prefill(bia, d, [0, 10, 5], [0, 10, 20], [1, 1]) == inv  # qo not monotone
+    assert call_prefill(bia, d, [1, 10], [0, 10], [1]) == inv  # qo_indptr[0] != 0
+    assert call_prefill(bia, d, [0, 10], [0, 5], [1]) == inv  # q_len > kv_len (causal)
+    assert call_prefill(bia, d, [0, 10], [0, 10], [0]) == inv  # last page length 0
+    assert call_prefill(bia, d, [0, 10], [0, 10], [1], split=100) == uns
+    assert call_prefill(bia, bia.make_desc(32, 8, 96, 1), [0, 10], [0, 10], [1]) == uns
+    assert call_prefill(bia, bia.make_desc(32, 6, 128, 1), [0, 10], [0, 10], [1]) == uns
+    assert call_prefill(bia, bia.make_desc(48, 3, 128, 1), [0, 10], [0, 10], [1]) == uns
+    assert call_prefill(bia, bia.make_desc(32, 8, 128, 3), [0, 10], [0, 10], [1]) == uns
+    assert call_prefill(bia, d, [0, 10], [0, 10], [1], ws_bytes=300) == small
+    assert call_prefill(bia, d, [0, 10], [0, 10], [1], ws=FAKE + 16) == inv  # unaligned
+    assert call_prefill(bia, d, [0, 10], [0, 10], [1], num_pages=0) == inv
+    lib = bia.load()
+    args = [None] * 20
+    args[4], args[12], args[13], args[14], args[16] = 0, 0, 0, 0, 0
+    assert lib.bia_prefill_paged(*args) == inv
+
+
+def test_decode_and_merge_reject_bad_arguments_on_the_host(bia):
+    lib = bia.load()
+    d = bia.make_desc(**QWEN)
+    p = ctypes.c_void_p
+    kvp = torch.tensor([0, 0], dtype=torch.int32)  # a request with no key
+    last = torch.tensor([1], dtype=torch.int32)
+    rc = lib.bia_decode_paged(ctypes.byref(d), p(FAKE), p(FAKE), p(FAKE), 1 << 20, p(FAKE),
+                              p(FAKE), p(FAKE), p(kvp.data_ptr()), p(last.data_ptr()), 1, 0,
+                              p(FAKE), 1 << 30, p(FAKE), None, None)
+    assert rc == bia.BIA_ERR_INVALID_ARG
+    assert lib.bia_merge_states(p(FAKE), p(FAKE), None, 4, 2, 8, 130, p(FAKE), None,
+                                None) == bia.BIA_ERR_UNSUPPORTED
+    assert lib.bia_merge_states(p(FAKE + 4), p(FAKE), None, 4, 2, 8, 128, p(FAKE), None,
+                                None) == bia.BIA_ERR_INVALID_ARG
+    assert lib.bia_merge_states(None, None, None, 0, 2, 8, 128, None, None, None) == bia.BIA_OK
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    import invariant_paged_attention_gb300 as m
+    saved = m._lib
+    m._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            m.load(str(tmp_path / "missing.so"))
+    finally:
+        m._lib = saved
