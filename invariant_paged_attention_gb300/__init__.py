@@ -178,10 +178,16 @@ def bia_read_status(workspace, stream=None) -> int:
 
 
 def bia_set_profile_events(begin=None, end=None):
-    """Record torch.cuda.Event `begin` / `end` around the attention kernel of
-    every later prefill / decode call (None, None: off)."""
-    h = (lambda e: None if e is None else ctypes.c_void_p(e.cuda_event))
-    load().bia_set_profile_events(h(begin), h(end))
+    """Record torch.cuda.Event `begin` / `end` (created with enable_timing)
+    around the attention kernel of every later prefill / decode call
+    (None, None: off)."""
+    def handle(e):
+        if e is None:
+            return None
+        if not e.cuda_event:  # torch creates the CUDA event on first record
+            e.record()
+        return ctypes.c_void_p(e.cuda_event)
+    load().bia_set_profile_events(handle(begin), handle(end))
 
 
 def bia_launch_count() -> int:
