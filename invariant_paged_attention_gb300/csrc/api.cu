@@ -49,7 +49,7 @@ int check_desc(const bia_attn_desc *d) {
 // planner will produce.  qo == nullptr: decode (one query per request).
 int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
               const int32_t *last, int32_t batch, int32_t causal, int32_t split, int tile_tokens,
-              HostPlan *hp) {
+              int tiles_per_unit, HostPlan *hp) {
   if (batch <= 0 || !kvp || !last) return BIA_ERR_INVALID_ARG;
   if (split <= 0 || split % bia::kKvBlock != 0) return BIA_ERR_UNSUPPORTED;
   if (qo && qo[0] != 0) return BIA_ERR_INVALID_ARG;
@@ -64,14 +64,9 @@ int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
     if (kv_len > INT32_MAX / 2) return BIA_ERR_UNSUPPORTED;
     if (causal && q_len > kv_len) return BIA_ERR_INVALID_ARG;
     if (!qo && kv_len == 0) return BIA_ERR_INVALID_ARG;
-    const int32_t tiles = static_cast<int32_t>((q_len + tile_tokens - 1) / tile_tokens);
     int32_t nsp = 1;
-    for (int32_t t = 0; t < tiles; ++t) {
-      const int32_t n = bia::tile_splits(static_cast<int32_t>(q_len), static_cast<int32_t>(kv_len),
-                                         t, tile_tokens, causal, split);
-      p.n_units += n;
-      if (n > nsp) nsp = n;
-    }
+    p.n_units += bia::request_units(static_cast<int32_t>(q_len), static_cast<int32_t>(kv_len),
+                                    tile_tokens, tiles_per_unit, causal, split, &nsp);
     if (nsp > 1) p.part_rows += q_len * nsp;
     p.total_q += q_len;
   }
@@ -105,10 +100,11 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
   const int G = desc->num_qo_heads / desc->num_kv_heads;
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
+  const int tiles_per_unit = decode ? 1 : bia::kPrefillTilesPerUnit;
   if (decode) causal = 1;
   HostPlan hp;
   rc = host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal, split,
-                 tile_tokens, &hp);
+                 tile_tokens, tiles_per_unit, &hp);
   if (rc != BIA_OK) return rc;
   const WsLayout w = bia::make_layout(batch, hp.n_units, hp.part_rows, desc->num_qo_heads,
                                       desc->head_dim);
@@ -125,6 +121,7 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   pa.batch = batch;
   pa.page_size = desc->page_size;
   pa.tile_tokens = tile_tokens;
+  pa.tiles_per_unit = tiles_per_unit;
   pa.causal = causal;
   pa.split = split;
   pa.n_units_expected = hp.n_units;
@@ -184,9 +181,10 @@ size_t workspace_size(bool decode, const bia_attn_desc *desc, const int32_t *qo_
   if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
   const int G = desc->num_qo_heads / desc->num_kv_heads;
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
+  const int tiles_per_unit = decode ? 1 : bia::kPrefillTilesPerUnit;
   HostPlan hp;
   if (host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, decode ? 1 : causal,
-                split, tile_tokens, &hp) != BIA_OK)
+                split, tile_tokens, tiles_per_unit, &hp) != BIA_OK)
     return 0;
   return bia::make_layout(batch, hp.n_units, hp.part_rows, desc->num_qo_heads, desc->head_dim)
       .total;

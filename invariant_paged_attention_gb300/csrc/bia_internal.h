@@ -17,6 +17,7 @@ constexpr int32_t kStatusTimeout = 4;      // a bounded device wait gave up
 
 constexpr int kTileRows = 128; // q tile rows (GQA-packed)
 constexpr int kKvBlock = 128;  // keys per block of the prefill inner loop
+constexpr int kPrefillTilesPerUnit = 2; // q tiles sharing one K/V stream in a prefill CTA
 
 // Per-request record written by the plan kernel.
 struct ReqInfo {
@@ -30,9 +31,10 @@ struct ReqInfo {
 };
 static_assert(sizeof(ReqInfo) == 32, "ReqInfo layout");
 
-// One unit of work: (request, q tile, split) for one kv head (grid.y).
+// One unit of work for one kv head (grid.y): q tiles tile .. tile+ntiles-1 of
+// request b against split-KV tile `split`.
 struct Unit {
-  int32_t b, tile, split, n_splits; // n_splits: split-KV tiles of this q tile
+  int32_t b, tile, split, ntiles;
 };
 
 // Byte offsets inside the caller's workspace.
@@ -63,6 +65,25 @@ __host__ __device__ inline int32_t tile_splits(int32_t q_len, int32_t kv_len, in
   return last < 0 ? 1 : last / split + 1;
 }
 
+// Units of one request: its q tiles grouped tiles_per_unit at a time, each
+// group crossed with the split tiles its last (widest) q tile touches.
+__host__ __device__ inline int64_t request_units(int32_t q_len, int32_t kv_len,
+                                                 int32_t tile_tokens, int32_t tiles_per_unit,
+                                                 int32_t causal, int32_t split,
+                                                 int32_t *max_splits) {
+  const int32_t tiles = (q_len + tile_tokens - 1) / tile_tokens;
+  int64_t units = 0;
+  int32_t nsp = 1;
+  for (int32_t t0 = 0; t0 < tiles; t0 += tiles_per_unit) {
+    const int32_t last = min(t0 + tiles_per_unit, tiles) - 1;
+    const int32_t n = tile_splits(q_len, kv_len, last, tile_tokens, causal, split);
+    units += n;
+    if (n > nsp) nsp = n;
+  }
+  if (max_splits) *max_splits = nsp;
+  return units;
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline WsLayout make_layout(int batch, int64_t n_units, int64_t part_rows, int Hq, int D) {
@@ -80,7 +101,7 @@ struct PlanArgs {
   const int32_t *qo_indptr;  // NULL for decode (one token per request)
   const int32_t *kv_indptr;
   const int32_t *kv_last_page_len;
-  int32_t batch, page_size, tile_tokens, causal, split;
+  int32_t batch, page_size, tile_tokens, tiles_per_unit, causal, split;
   int64_t n_units_expected, part_rows_expected;
   int32_t *status;
   ReqInfo *reqs;

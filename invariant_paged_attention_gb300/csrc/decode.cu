@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (G <= 4 ? 2 : 1))
     const float val = empty ? 0.f : __fdiv_rn(O, L);
     const float lse = empty ? -INFINITY : __fmul_rn(__fadd_rn(M, lg2(L)), kLn2);
     const int64_t row = static_cast<int64_t>(r.q_start) * a.Hq + h;
-    if (u.n_splits == 1) {
+    if ((r.kv_len - 1) / a.split == 0) { // a single split: final row
       a.out[row * D + d] = to_bf16(val);
       if (a.lse && d == 0) a.lse[row] = lse;
     } else {

@@ -32,13 +32,8 @@ __device__ inline void request_geometry(const PlanArgs &a, int b, int32_t &q_sta
 __device__ inline ReqCounts request_counts(const PlanArgs &a, int32_t q_len, int32_t kv_len,
                                            int32_t &nsp) {
   ReqCounts c{0, 0};
-  const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
-  nsp = 1;
-  for (int32_t t = 0; t < tiles; ++t) {
-    const int32_t n = tile_splits(q_len, kv_len, t, a.tile_tokens, a.causal, a.split);
-    c.units += n;
-    if (n > nsp) nsp = n;
-  }
+  c.units = request_units(q_len, kv_len, a.tile_tokens, a.tiles_per_unit, a.causal, a.split,
+                          &nsp);
   if (nsp > 1) c.rows = static_cast<int64_t>(q_len) * nsp;
   return c;
 }
@@ -99,10 +94,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     r.pad = 0;
     a.reqs[b] = r;
     const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
+    const int32_t groups = (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
     // last q tiles first: they carry the most keys
-    for (int32_t t = tiles - 1; t >= 0; --t) {
-      const int32_t n = tile_splits(q_len, kv_len, t, a.tile_tokens, a.causal, a.split);
-      for (int32_t s = 0; s < n; ++s) a.units[unit++] = Unit{b, t, s, n};
+    for (int32_t gi = groups - 1; gi >= 0; --gi) {
+      const int32_t t0 = gi * a.tiles_per_unit;
+      const int32_t nt = min(a.tiles_per_unit, tiles - t0);
+      const int32_t n = tile_splits(q_len, kv_len, t0 + nt - 1, a.tile_tokens, a.causal, a.split);
+      for (int32_t s = 0; s < n; ++s) a.units[unit++] = Unit{b, t0, s, nt};
     }
     row += c.rows;
   }
