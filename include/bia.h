@@ -135,6 +135,7 @@ BIA_API size_t bia_decode_workspace_size(const bia_attn_desc *desc, const int32_
                                  const int32_t *kv_last_page_len_host, int32_t batch,
                                  int32_t split_size);
 
+
 /*
  * Fixed-order log-sum-exp merge of attention states (the merge the split-KV
  * partials of "sglang PR #10417", Modifications, need; the pages fix only
@@ -162,6 +163,10 @@ BIA_API int32_t bia_q_tile_tokens(int32_t gqa_group);
 
 /* Static text for a bia_status value. */
 BIA_API const char *bia_status_string(int status);
+
+/* Detail of the last BIA_ERR_CUDA returned in the calling thread (the CUDA
+ * or driver call that failed and its error); empty if none. */
+BIA_API const char *bia_last_error(void);
 
 /*
  * Copies the device status word of the last call that used `workspace`

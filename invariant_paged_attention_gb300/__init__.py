@@ -32,13 +32,16 @@ BIA_DECODE_SPLIT = 2048
 EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged",
            "bia_decode_workspace_size", "bia_merge_states", "bia_q_tile_tokens",
            "bia_status_string", "bia_read_status", "bia_set_profile_events",
-           "bia_launch_count")
+           "bia_launch_count", "bia_last_error")
 
 
 class BiaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where} failed: {status_string(status)} ({status})")
+        detail = ""
+        if status == BIA_ERR_CUDA:
+            detail = ": " + load().bia_last_error().decode()
+        super().__init__(f"{where} failed: {status_string(status)} ({status}){detail}")
 
 
 class AttnDesc(ctypes.Structure):
@@ -83,6 +86,8 @@ def load(path: str = LIB_PATH):
     lib.bia_set_profile_events.restype = None
     lib.bia_launch_count.argtypes = []
     lib.bia_launch_count.restype = ctypes.c_uint64
+    lib.bia_last_error.argtypes = []
+    lib.bia_last_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 

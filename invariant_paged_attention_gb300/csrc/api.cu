@@ -4,7 +4,10 @@
 // synchronisation (except bia_read_status, which exists to synchronise).
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
+
+#include <cudaTypedefs.h>
 
 #include "../../include/bia.h"
 #include "bia_internal.h"
@@ -13,12 +16,23 @@ namespace {
 
 cudaEvent_t g_attn_begin = nullptr, g_attn_end = nullptr;
 unsigned long long g_launches = 0;
+thread_local char g_last_error[256] = "";
+
+int fail(int status, const char *what, int code) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s (code %d)", what, code);
+  return status;
+}
+int cuda_fail(const char *what, cudaError_t e) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s: %s", what, cudaGetErrorString(e));
+  return BIA_ERR_CUDA;
+}
 
 using bia::PlanArgs;
 using bia::AttnArgs;
 using bia::WsLayout;
 
 struct HostPlan {
+  int64_t n_groups = 0;
   int64_t n_units = 0;
   int64_t part_rows = 0;
   int64_t total_q = 0;
@@ -65,6 +79,8 @@ int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
     if (causal && q_len > kv_len) return BIA_ERR_INVALID_ARG;
     if (!qo && kv_len == 0) return BIA_ERR_INVALID_ARG;
     int32_t nsp = 1;
+    const int64_t tiles = (q_len + tile_tokens - 1) / tile_tokens;
+    p.n_groups += (tiles + tiles_per_unit - 1) / tiles_per_unit;
     p.n_units += bia::request_units(static_cast<int32_t>(q_len), static_cast<int32_t>(kv_len),
                                     tile_tokens, tiles_per_unit, causal, split, &nsp);
     if (nsp > 1) p.part_rows += q_len * nsp;
@@ -73,6 +89,39 @@ int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
   if (p.n_units > INT32_MAX) return BIA_ERR_UNSUPPORTED; // grid.x limit is 2^31-1
   *hp = p;
   return BIA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no direct
+// link against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// A 2-D map over `rows` rows of `head_dim` bf16 (row pitch head_dim*2 bytes),
+// 64-column x 1-row boxes with the 128-byte swizzle of the MMA operand tiles;
+// coordinates outside the map read as zeros.
+int encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return -1;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return static_cast<int>(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
 float effective_scale(const bia_attn_desc *d) {
@@ -106,10 +155,14 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   rc = host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal, split,
                  tile_tokens, tiles_per_unit, &hp);
   if (rc != BIA_OK) return rc;
-  const WsLayout w = bia::make_layout(batch, hp.n_units, hp.part_rows, desc->num_qo_heads,
-                                      desc->head_dim);
+  const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows,
+                                      desc->num_qo_heads, desc->head_dim);
   if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
   if (hp.total_q == 0) return BIA_OK;
+
+  const int64_t q_rows = hp.total_q * desc->num_qo_heads;
+  const int64_t kv_rows = num_pages * desc->page_size * desc->num_kv_heads;
+  if (!decode && (q_rows >= INT32_MAX || kv_rows >= INT32_MAX)) return BIA_ERR_UNSUPPORTED;
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -124,12 +177,16 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   pa.tiles_per_unit = tiles_per_unit;
   pa.causal = causal;
   pa.split = split;
+  pa.n_groups_expected = hp.n_groups;
   pa.n_units_expected = hp.n_units;
   pa.part_rows_expected = hp.part_rows;
   pa.status = reinterpret_cast<int32_t *>(ws + w.status);
   pa.reqs = reinterpret_cast<bia::ReqInfo *>(ws + w.reqs);
+  pa.group_off = reinterpret_cast<int32_t *>(ws + w.group_off);
+  pa.group_cnt = reinterpret_cast<int32_t *>(ws + w.group_cnt);
   pa.units = reinterpret_cast<bia::Unit *>(ws + w.units);
-  if (bia::launch_plan(pa, st) != cudaSuccess) return BIA_ERR_CUDA;
+  cudaError_t pe = bia::launch_plan(pa, st);
+  if (pe != cudaSuccess) return cuda_fail("plan kernel launch", pe);
   __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
 
   AttnArgs a{};
@@ -158,16 +215,24 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   a.out = static_cast<uint16_t *>(out);
   a.lse = lse;
   a.status = pa.status;
+  if (!decode) {
+    a.q_rows = static_cast<int32_t>(q_rows);
+    a.kv_rows = static_cast<int32_t>(kv_rows);
+    int ce = encode_rows_map(&a.tm_q, q, q_rows, desc->head_dim);
+    if (ce == 0) ce = encode_rows_map(&a.tm_k, k_cache, kv_rows, desc->head_dim);
+    if (ce == 0) ce = encode_rows_map(&a.tm_v, v_cache, kv_rows, desc->head_dim);
+    if (ce != 0) return fail(BIA_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable", ce);
+  }
 
   const bool profile = g_attn_begin != nullptr && g_attn_end != nullptr;
   if (profile && cudaEventRecord(g_attn_begin, st) != cudaSuccess) return BIA_ERR_CUDA;
   cudaError_t e = decode ? bia::launch_decode(a, st) : bia::launch_prefill(a, st);
-  if (e != cudaSuccess) return BIA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(decode ? "decode kernel launch" : "prefill kernel launch", e);
   if (hp.n_units > 0) __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   if (profile && cudaEventRecord(g_attn_end, st) != cudaSuccess) return BIA_ERR_CUDA;
   if (hp.part_rows > 0) {
     e = bia::launch_merge_partials(a, st);
-    if (e != cudaSuccess) return BIA_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
     __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   }
   return BIA_OK;
@@ -186,7 +251,8 @@ size_t workspace_size(bool decode, const bia_attn_desc *desc, const int32_t *qo_
   if (host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, decode ? 1 : causal,
                 split, tile_tokens, tiles_per_unit, &hp) != BIA_OK)
     return 0;
-  return bia::make_layout(batch, hp.n_units, hp.part_rows, desc->num_qo_heads, desc->head_dim)
+  return bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows, desc->num_qo_heads,
+                          desc->head_dim)
       .total;
 }
 
@@ -282,5 +348,7 @@ void bia_set_profile_events(void *attn_begin, void *attn_end) {
 }
 
 uint64_t bia_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+const char *bia_last_error(void) { return g_last_error; }
 
 } // extern "C"

@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h> // CUtensorMap (a plain 128-byte struct; no driver-library link needed)
 #include <cuda_runtime.h>
 
 namespace bia {
@@ -41,6 +42,8 @@ struct Unit {
 struct WsLayout {
   size_t status = 0;   // int32[64]
   size_t reqs = 0;     // ReqInfo[batch]
+  size_t group_off = 0; // int32[batch + 1]: first q-tile group of each request
+  size_t group_cnt = 0; // int32[n_groups]: first unit of each group
   size_t units = 0;    // Unit[n_units]
   size_t part_o = 0;   // float[part_rows * Hq * D]
   size_t part_lse = 0; // float[part_rows * Hq]
@@ -86,11 +89,14 @@ __host__ __device__ inline int64_t request_units(int32_t q_len, int32_t kv_len,
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout make_layout(int batch, int64_t n_units, int64_t part_rows, int Hq, int D) {
+inline WsLayout make_layout(int batch, int64_t n_groups, int64_t n_units, int64_t part_rows,
+                            int Hq, int D) {
   WsLayout w;
   w.status = 0;
   w.reqs = 256;
-  w.units = align_up(w.reqs + sizeof(ReqInfo) * (size_t)batch, 256);
+  w.group_off = align_up(w.reqs + sizeof(ReqInfo) * (size_t)batch, 256);
+  w.group_cnt = align_up(w.group_off + sizeof(int32_t) * ((size_t)batch + 1), 256);
+  w.units = align_up(w.group_cnt + sizeof(int32_t) * (size_t)n_groups, 256);
   w.part_o = align_up(w.units + sizeof(Unit) * (size_t)n_units, 256);
   w.part_lse = align_up(w.part_o + sizeof(float) * (size_t)part_rows * Hq * D, 256);
   w.total = align_up(w.part_lse + sizeof(float) * (size_t)part_rows * Hq, 256);
@@ -102,9 +108,10 @@ struct PlanArgs {
   const int32_t *kv_indptr;
   const int32_t *kv_last_page_len;
   int32_t batch, page_size, tile_tokens, tiles_per_unit, causal, split;
-  int64_t n_units_expected, part_rows_expected;
+  int64_t n_groups_expected, n_units_expected, part_rows_expected;
   int32_t *status;
   ReqInfo *reqs;
+  int32_t *group_off, *group_cnt;
   Unit *units;
 };
 
@@ -125,6 +132,10 @@ struct AttnArgs {
   uint16_t *out;
   float *lse;
   int32_t *status;
+  // TMA descriptors (prefill): q rows [total_q*Hq, D] and key / value rows
+  // [num_pages*page_size*Hkv, D], 64-column boxes, one row high, SW128
+  CUtensorMap tm_q, tm_k, tm_v;
+  int32_t q_rows, kv_rows; // row extents of the maps (a row >= extent reads as zeros)
 };
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);

@@ -1,12 +1,18 @@
 // Split-KV paged decode: one CTA per (request, split-KV tile, kv head).
 //
-// The G query heads that share a kv head are kept in registers; the split's
-// keys stream through the CTA as 16-byte vector loads, D/8 lanes per key row
-// so every 32-byte sector of a row is consumed by one load instruction.  Each
-// lane group keeps an online softmax state for the keys it owns (a fixed
-// function of the key index), and the 8 warps' states are combined in a
-// fixed order at the end.  Nothing depends on the grid, so a request's
-// partial (and its output) has the same bits in any batch.
+// The split's keys are cut into chunks of 8 consecutive keys; warp w of the
+// CTA owns chunks w, w+8, w+16, ...  Each warp streams its chunks' key and
+// value rows from the paged cache into its own ring of shared-memory stages
+// with bulk asynchronous copies (one cp.async.bulk per 2*D-byte row, issued by
+// 16 lanes, completion counted on the stage's mbarrier), keeping several
+// kilobytes per warp in flight without holding registers; the page index of
+// the next chunk is fetched one chunk ahead.  D/8 lanes read one row (16
+// bytes each).  The G query heads of the kv head stay in registers as fp32
+// pairs, pre-scaled by sm_scale * log2 e, and Q.K and P.V run on packed
+// fp32x2 FMAs.  Every lane group keeps an online softmax per head over its own
+// keys (a fixed function of the key index), rescaled lazily when its max grows
+// by more than 2^8; lane groups and then warps are combined in a fixed order,
+// so a request's partial and output have the same bits in any batch.
 //
 // The fixed split of 2048 keys per tile and the merge of the tiles' partials
 // follow "sglang PR #10417 [POC] Support deterministic inference",
@@ -18,36 +24,76 @@ namespace bia {
 
 namespace {
 
-constexpr int kDecodeWarps = 8;
-constexpr int kDecodeSteps = 4; // key rows per lane group per iteration
+constexpr int kWarps = 8;
+constexpr int kThreadsDec = kWarps * 32;
+constexpr int kChunk = 8;              // keys per chunk
+constexpr float kLazyThreshold = 8.0f; // log2 units
 
-__device__ __forceinline__ uint4 ld_stream(const uint16_t *p) {
+template <int D>
+struct DecSmem {
+  static constexpr int kStages = D == 128 ? 3 : 5;
+  static constexpr int kRow = D * 2;                  // bytes of one key row
+  static constexpr int kStage = 2 * kChunk * kRow;    // K rows then V rows
+  static constexpr int kRing = kStages * kStage;      // one warp's ring
+  static constexpr int kBar = kWarps * kRing;         // mbarriers [warp][stage]
+  static constexpr int kBytes = kBar + kWarps * kStages * 8;
+  static constexpr int kAlloc = kBytes + 128;
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "r"(addr));
   return r;
 }
 
-__device__ __forceinline__ void unpack8(const uint4 w, float (&f)[8]) {
-  f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x);
-  f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
-  f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
-  f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+// Sums each of the G partial scores over the LPK lanes of a key group and
+// leaves all G totals on every lane of the group (identical bits on each).
+template <int G, int LPK>
+__device__ __forceinline__ void group_reduce(float (&s)[G]) {
+  if constexpr (G == 4 && LPK == 16) {
+    const int sub = threadIdx.x & 15;
+    const bool b3 = (sub >> 3) & 1, b2 = (sub >> 2) & 1;
+    // reduce-scatter: the lane keeps heads {2*b3, 2*b3+1}, then head 2*b3+b2
+    const float kx = b3 ? s[2] : s[0], ky = b3 ? s[3] : s[1];
+    const float sx = b3 ? s[0] : s[2], sy = b3 ? s[1] : s[3];
+    const float px = kx + __shfl_xor_sync(0xffffffffu, sx, 8);
+    const float py = ky + __shfl_xor_sync(0xffffffffu, sy, 8);
+    float c = (b2 ? py : px) + __shfl_xor_sync(0xffffffffu, b2 ? px : py, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    // all-gather: c is head 2*b3 + b2
+    const float d = __shfl_xor_sync(0xffffffffu, c, 4); // head 2*b3 + !b2
+    const float e = __shfl_xor_sync(0xffffffffu, c, 8); // head 2*!b3 + b2
+    const float f = __shfl_xor_sync(0xffffffffu, d, 8); // head 2*!b3 + !b2
+    const float lo = b2 ? d : c, hi = b2 ? c : d;        // heads 2*b3, 2*b3+1
+    const float lo2 = b2 ? f : e, hi2 = b2 ? e : f;      // heads 2*!b3, 2*!b3+1
+    s[0] = b3 ? lo2 : lo;
+    s[1] = b3 ? hi2 : hi;
+    s[2] = b3 ? lo : lo2;
+    s[3] = b3 ? hi : hi2;
+  } else {
+#pragma unroll
+    for (int off = 1; off < LPK; off <<= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g) s[g] += __shfl_xor_sync(0xffffffffu, s[g], off);
+  }
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kDecodeWarps * 32, (G <= 4 ? 2 : 1))
+__global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     decode_kernel(const AttnArgs a) {
-  constexpr int LPK = D / 8;        // lanes per key row
-  constexpr int KPW = 32 / LPK;     // key rows per warp per load step
-  constexpr int U = kDecodeSteps;
-  constexpr int KEYS_PER_ITER = kDecodeWarps * KPW * U;
-  constexpr int NSTATE = kDecodeWarps; // one combined state per warp
+  using L = DecSmem<D>;
+  constexpr int LPK = D / 8;         // lanes per key row
+  constexpr int KPW = 32 / LPK;      // key rows per warp step
+  constexpr int STEPS = kChunk / KPW; // steps per chunk
+  constexpr int NS = L::kStages;
 
-  __shared__ float s_m[NSTATE][G];
-  __shared__ float s_l[NSTATE][G];
-  __shared__ __align__(16) float s_o[NSTATE][G][D];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  const uint32_t sbase = smem_u32(smem);
 
   if (blockIdx.x >= a.n_units) return;
   const Unit u = a.units[blockIdx.x];
@@ -58,110 +104,140 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (G <= 4 ? 2 : 1))
   const int grp = lane / LPK, sub = lane % LPK;
   const int32_t key_begin = u.split * a.split;
   const int32_t key_end = min(key_begin + a.split, r.kv_len);
+  const int n_chunks = (key_end - key_begin + kChunk - 1) / kChunk;
+  const int my_chunks = warp < n_chunks ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
 
-  // queries of the group, pre-scaled by sm_scale * log2(e)
-  float q[G][8];
+  const uint32_t ring = sbase + warp * L::kRing;
+  auto bar = [&](int s) { return sbase + L::kBar + 8u * (warp * NS + s); };
+  auto sK = [&](int s) { return ring + s * L::kStage; };
+  auto sV = [&](int s) { return ring + s * L::kStage + kChunk * L::kRow; };
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(bar(s), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // ---- chunk loads: lanes 0..7 copy key rows, 8..15 the value rows of the
+  // same keys; rows past the split or on a bad page are zero-filled instead
+  const int kl_ld = lane & 7;
+  const int page_mask = (1 << a.page_shift) - 1;
+  auto page_of = [&](int i) -> int32_t { // page index of this lane's key in chunk i
+    const int32_t key = key_begin + (warp + kWarps * i) * kChunk + kl_ld;
+    if (lane >= 16 || i >= my_chunks || key >= key_end) return -1;
+    return __ldg(a.kv_indices + r.page_base + (key >> a.page_shift));
+  };
+  int32_t pg_next = page_of(0);
+  auto issue = [&](int i) {
+    const int st = i % NS;
+    const int32_t pg = pg_next;
+    pg_next = page_of(i + 1);
+    const int32_t key = key_begin + (warp + kWarps * i) * kChunk + kl_ld;
+    bool ok = lane < 16 && key < key_end;
+    if (ok && (pg < 0 || pg >= a.num_pages)) {
+      atomicOr(a.status, kStatusBadPage);
+      ok = false;
+    }
+    const uint32_t dst = (lane < 8 ? sK(st) : sV(st)) + kl_ld * L::kRow;
+    if (lane < 16 && !ok) {
+#pragma unroll
+      for (int b = 0; b < L::kRow; b += 16)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + b), "r"(0) : "memory");
+    }
+    const int n_ok = __popc(__ballot_sync(0xffffffffu, ok));
+    __syncwarp();
+    if (lane == 0) mbar_expect_tx(bar(st), static_cast<uint32_t>(n_ok) * L::kRow);
+    __syncwarp();
+    if (ok) {
+      const int64_t off =
+          (((static_cast<int64_t>(pg) << a.page_shift) + (key & page_mask)) * a.Hkv + kvh) * D;
+      bulk_g2s(dst, (lane < 8 ? a.k_cache : a.v_cache) + off, L::kRow, bar(st));
+    }
+  };
+  for (int i = 0; i < NS && i < my_chunks; ++i) issue(i);
+
+  // ---- queries of the group as fp32 pairs, pre-scaled by sm_scale * log2(e)
+  uint64_t q2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const uint16_t *src =
-        a.q + (static_cast<int64_t>(r.q_start) * a.Hq + kvh * G + g) * D + sub * 8;
-    float f[8];
-    unpack8(*reinterpret_cast<const uint4 *>(src), f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[g][i] = f[i] * a.scale_log2;
+    const uint4 w = *reinterpret_cast<const uint4 *>(
+        a.q + (static_cast<int64_t>(r.q_start) * a.Hq + kvh * G + g) * D + sub * 8);
+    const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2);
+    q2[g][0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
+    q2[g][1] = fmul2(bf16x2_to_f32x2(w.y), sc2);
+    q2[g][2] = fmul2(bf16x2_to_f32x2(w.z), sc2);
+    q2[g][3] = fmul2(bf16x2_to_f32x2(w.w), sc2);
   }
-
-  float m[G], l[G], o[G][8];
+  float m[G], l[G];
+  uint64_t o2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m[g] = -INFINITY;
     l[g] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[g][i] = 0.f;
+    for (int k = 0; k < 4; ++k) o2[g][k] = 0;
   }
 
-  const int page_mask = (1 << a.page_shift) - 1;
-  for (int32_t it = key_begin; it < key_end; it += KEYS_PER_ITER) {
-    uint4 kw[U], vw[U];
-    bool ok[U];
-#pragma unroll
-    for (int s = 0; s < U; ++s) {
-      const int32_t key = it + (warp * U + s) * KPW + grp;
-      ok[s] = key < key_end;
-      int64_t off = 0;
-      if (ok[s]) {
-        const int32_t page = __ldg(a.kv_indices + r.page_base + (key >> a.page_shift));
-        if (page < 0 || page >= a.num_pages) {
-          atomicOr(a.status, kStatusBadPage);
-          ok[s] = false;
-        } else {
-          off = ((static_cast<int64_t>(page) << a.page_shift) + (key & page_mask)) * a.Hkv + kvh;
-          off = off * D + sub * 8;
-        }
-      }
-      if (ok[s]) {
-        kw[s] = ld_stream(a.k_cache + off);
-        vw[s] = ld_stream(a.v_cache + off);
-      } else {
-        kw[s] = make_uint4(0, 0, 0, 0);
-        vw[s] = make_uint4(0, 0, 0, 0);
-      }
+  bool failed = false;
+  for (int i = 0; i < my_chunks; ++i) {
+    const int st = i % NS;
+    if (!mbar_wait(bar(st), (i / NS) & 1, a.status)) {
+      failed = true;
+      break;
     }
-    // scores
-    float sc[U][G];
+    const int32_t key0 = key_begin + (warp + kWarps * i) * kChunk;
 #pragma unroll
-    for (int s = 0; s < U; ++s) {
-      float kf[8];
-      unpack8(kw[s], kf);
+    for (int s = 0; s < STEPS; ++s) {
+      const int kl = s * KPW + grp; // row of the chunk
+      const uint4 kw = lds128(sK(st) + kl * L::kRow + sub * 16);
+      const uint4 vw = lds128(sV(st) + kl * L::kRow + sub * 16);
+      const uint64_t k2[4] = {bf16x2_to_f32x2(kw.x), bf16x2_to_f32x2(kw.y),
+                              bf16x2_to_f32x2(kw.z), bf16x2_to_f32x2(kw.w)};
+      float sc[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float acc = 0.f;
+        uint64_t acc = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc = fmaf(q[g][i], kf[i], acc);
-        sc[s][g] = acc;
+        for (int k = 0; k < 4; ++k) ffma2(acc, q2[g][k], k2[k]);
+        float x, y;
+        f32x2_split(acc, x, y);
+        sc[g] = x + y;
+      }
+      group_reduce<G, LPK>(sc);
+      if (key0 + kl >= key_end) continue; // past the split's last key
+      const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
+                              bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
+      // online softmax with lazy rescale: the running max moves only when a
+      // score exceeds it by more than 2^8 (a function of this lane group's own
+      // keys, so the result is the same in any batch)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (sc[g] > m[g] + kLazyThreshold || m[g] == -INFINITY) {
+          const float alpha = ex2(m[g] - sc[g]);
+          l[g] *= alpha;
+          const uint64_t a2 = f32x2(alpha, alpha);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
+          m[g] = sc[g];
+        }
+        const float p = ex2(sc[g] - m[g]);
+        l[g] += p;
+        const uint64_t p2 = f32x2(p, p);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
       }
     }
-#pragma unroll
-    for (int off = 1; off < LPK; off <<= 1) {
-#pragma unroll
-      for (int s = 0; s < U; ++s)
-#pragma unroll
-        for (int g = 0; g < G; ++g) sc[s][g] += __shfl_xor_sync(0xffffffffu, sc[s][g], off);
-    }
-    // online softmax over this lane group's U keys
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float mx = m[g];
-#pragma unroll
-      for (int s = 0; s < U; ++s) {
-        if (!ok[s]) sc[s][g] = -INFINITY;
-        mx = fmaxf(mx, sc[s][g]);
-      }
-      if (mx == -INFINITY) continue;
-      const float alpha = ex2(m[g] - mx);
-      float psum = 0.f;
-      float p[U];
-#pragma unroll
-      for (int s = 0; s < U; ++s) {
-        p[s] = ex2(sc[s][g] - mx);
-        psum += p[s];
-      }
-      l[g] = fmaf(l[g], alpha, psum);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[g][i] *= alpha;
-      m[g] = mx;
-#pragma unroll
-      for (int s = 0; s < U; ++s) {
-        float vf[8];
-        unpack8(vw[s], vf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[g][i] = fmaf(p[s], vf[i], o[g][i]);
-      }
-    }
+    __syncwarp();
+    fence_proxy_async(); // this warp's reads of the stage precede the refill
+    if (i + NS < my_chunks) issue(i + NS);
   }
 
-  // combine the KPW lane groups of the warp (butterfly; lane group 0 keeps
-  // the result that is published)
+  float o[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f32x2_split(o2[g][k], o[g][2 * k], o[g][2 * k + 1]);
+
+  // combine the KPW lane groups of the warp (butterfly: identical on every lane)
 #pragma unroll
   for (int off = LPK; off < 32; off <<= 1) {
 #pragma unroll
@@ -171,49 +247,54 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (G <= 4 ? 2 : 1))
       const float M = fmaxf(m[g], mo);
       const float w1 = M == -INFINITY ? 0.f : ex2(m[g] - M);
       const float w2 = M == -INFINITY ? 0.f : ex2(mo - M);
-      l[g] = fmaf(l[g], w1, lo * w2);
+      l[g] = l[g] * w1 + lo * w2;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float oo = __shfl_xor_sync(0xffffffffu, o[g][i], off);
-        o[g][i] = fmaf(o[g][i], w1, oo * w2);
+      for (int k = 0; k < 8; ++k) {
+        const float oo = __shfl_xor_sync(0xffffffffu, o[g][k], off);
+        o[g][k] = o[g][k] * w1 + oo * w2;
       }
       m[g] = M;
     }
   }
+  // every ring has drained: reuse the shared memory for the warp states
+  __syncthreads();
+  float *s_m = reinterpret_cast<float *>(smem);
+  float *s_l = s_m + kWarps * G;
+  float *s_o = s_l + kWarps * G; // [warp][g][D]
   if (grp == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       if (sub == 0) {
-        s_m[warp][g] = m[g];
-        s_l[warp][g] = l[g];
+        s_m[warp * G + g] = failed ? -INFINITY : m[g];
+        s_l[warp * G + g] = l[g];
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s_o[warp][g][sub * 8 + i] = o[g][i];
+      for (int k = 0; k < 8; ++k) s_o[(warp * G + g) * D + sub * 8 + k] = o[g][k];
     }
   }
   __syncthreads();
 
-  // combine the NSTATE states in index order; thread handles (g, d) pairs
-  for (int e = threadIdx.x; e < G * D; e += kDecodeWarps * 32) {
+  const bool single = (r.kv_len - 1) / a.split == 0; // one split: the final row
+  for (int e = threadIdx.x; e < G * D; e += kThreadsDec) {
     const int g = e / D, d = e % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < NSTATE; ++k) M = fmaxf(M, s_m[k][g]);
-    float L = 0.f, O = 0.f;
+    for (int k = 0; k < kWarps; ++k) M = fmaxf(M, s_m[k * G + g]);
+    float Ls = 0.f, O = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int k = 0; k < NSTATE; ++k) {
-        const float w = ex2(s_m[k][g] - M);
-        L = fmaf(s_l[k][g], w, L);
-        O = fmaf(s_o[k][g][d], w, O);
+      for (int k = 0; k < kWarps; ++k) {
+        const float w = ex2(s_m[k * G + g] - M);
+        Ls = fmaf(s_l[k * G + g], w, Ls);
+        O = fmaf(s_o[(k * G + g) * D + d], w, O);
       }
     }
     const int h = kvh * G + g;
-    const bool empty = !(L > 0.f);
-    const float val = empty ? 0.f : __fdiv_rn(O, L);
-    const float lse = empty ? -INFINITY : __fmul_rn(__fadd_rn(M, lg2(L)), kLn2);
+    const bool empty_row = !(Ls > 0.f);
+    const float val = empty_row ? 0.f : __fdiv_rn(O, Ls);
+    const float lse = empty_row ? -INFINITY : __fmul_rn(__fadd_rn(M, lg2(Ls)), kLn2);
     const int64_t row = static_cast<int64_t>(r.q_start) * a.Hq + h;
-    if ((r.kv_len - 1) / a.split == 0) { // a single split: final row
+    if (single) {
       a.out[row * D + d] = to_bf16(val);
       if (a.lse && d == 0) a.lse[row] = lse;
     } else {
@@ -224,18 +305,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (G <= 4 ? 2 : 1))
   }
 }
 
+template <int D, int G>
+cudaError_t launch_decode_dg(const AttnArgs &a, cudaStream_t s) {
+  using L = DecSmem<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(static_cast<unsigned>(a.n_units), static_cast<unsigned>(a.Hkv));
+  decode_kernel<D, G><<<grid, kThreadsDec, L::kAlloc, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_decode_d(const AttnArgs &a, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(a.n_units), static_cast<unsigned>(a.Hkv));
-  dim3 block(kDecodeWarps * 32);
   switch (a.G) {
-  case 1: decode_kernel<D, 1><<<grid, block, 0, s>>>(a); break;
-  case 2: decode_kernel<D, 2><<<grid, block, 0, s>>>(a); break;
-  case 4: decode_kernel<D, 4><<<grid, block, 0, s>>>(a); break;
-  case 8: decode_kernel<D, 8><<<grid, block, 0, s>>>(a); break;
+  case 1: return launch_decode_dg<D, 1>(a, s);
+  case 2: return launch_decode_dg<D, 2>(a, s);
+  case 4: return launch_decode_dg<D, 4>(a, s);
+  case 8: return launch_decode_dg<D, 8>(a, s);
   default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 } // namespace

@@ -60,17 +60,16 @@ __device__ __forceinline__ int owner(const int32_t *qo_indptr, int batch, int64_
   return lo;
 }
 
-// Merge of the split partials a prefill / decode call left in the workspace.
-// Rows whose q tile had one split were written by the attention kernel.
+// Merge of the split partials a prefill / decode call left in the workspace:
+// one warp per q token, looping over its q heads.  Rows whose q tile had a
+// single split were written by the attention kernel and are skipped.
 template <int V>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_partials_kernel(const AttnArgs a) {
   const int D = a.D;
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
-  if (row >= a.total_rows * a.Hq) return;
-  const int64_t token = row / a.Hq;
-  const int h = static_cast<int>(row - token * a.Hq);
+  const int64_t token = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (token >= a.total_rows) return;
   const int b = a.qo_indptr ? owner(a.qo_indptr, a.batch, token) : static_cast<int>(token);
   const ReqInfo r = a.reqs[b];
   const int32_t t = static_cast<int32_t>(token - r.q_start);
@@ -79,24 +78,27 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   if (n_tile <= 1 || r.rowbase < 0) return;
   const int32_t p = a.causal ? r.kv_len - r.q_len + t : r.kv_len - 1;
   const int32_t n_row = min(n_tile, p / a.split + 1);
-  const int64_t base = (r.rowbase + static_cast<int64_t>(t) * r.nsp) * a.Hq + h;
-  float L = -INFINITY;
-  float o[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) o[i] = 0.f;
-  for (int s = 0; s < n_row; ++s) {
-    const int64_t idx = base + static_cast<int64_t>(s) * a.Hq;
-    const float ls = __ldg(a.part_lse + idx);
-    if (ls == -INFINITY) continue;
-    float v[V];
-    load_state<V>(a.part_o + idx * D, D, lane, v);
-    fold_state<V>(L, o, ls, v);
-  }
-  if (L == -INFINITY) {
+  const int64_t base = (r.rowbase + static_cast<int64_t>(t) * r.nsp) * a.Hq;
+  for (int h = 0; h < a.Hq; ++h) {
+    float L = -INFINITY;
+    float o[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) o[i] = 0.f;
+    for (int s = 0; s < n_row; ++s) {
+      const int64_t idx = base + static_cast<int64_t>(s) * a.Hq + h;
+      const float ls = __ldg(a.part_lse + idx);
+      if (ls == -INFINITY) continue;
+      float v[V];
+      load_state<V>(a.part_o + idx * D, D, lane, v);
+      fold_state<V>(L, o, ls, v);
+    }
+    if (L == -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) o[i] = 0.f;
+    }
+    const int64_t row = token * a.Hq + h;
+    store_row<V>(a.out + row * D, D, a.lse ? a.lse + row : nullptr, lane, L, o);
   }
-  store_row<V>(a.out + row * D, D, a.lse ? a.lse + row : nullptr, lane, L, o);
 }
 
 // Public merge: v [n, S, H, D], s [n, S, H], optional per-row counts.
@@ -134,9 +136,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 } // namespace
 
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t st) {
-  const int64_t rows = a.total_rows * a.Hq;
-  if (rows == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
+  if (a.total_rows == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>((a.total_rows + kMergeWarps - 1) / kMergeWarps);
   merge_partials_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(a);
   return cudaGetLastError();
 }

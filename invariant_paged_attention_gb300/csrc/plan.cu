@@ -1,8 +1,17 @@
 // Device-side planner: turns the caller's indptr arrays into per-request
-// records and the list of work units (request, q tile, split-KV tile), so no
-// plan ever travels from host to device.  One CTA; it also clears the status
-// word.  The host sizes the launch from its mirrors of the same arrays; when
-// the device arrays disagree, every unit is disabled and a status bit is set
+// records and the list of work units (request, group of q tiles, split-KV
+// tile), so no plan ever travels from host to device.  One CTA; it also clears
+// the status word.
+//
+//   A. per request: lengths, q-tile groups, split tiles of the widest tile,
+//      partial rows; block scans give group offsets and partial-row bases
+//   B. per group (all threads): its split count
+//   C. block scan of the split counts: each group's first unit
+//   D. per group: its units (the request's last groups first: they carry the
+//      most keys)
+//
+// The host sizes the launch from its mirrors of the same arrays; when the
+// device arrays disagree, every unit is disabled and a status bit is set
 // instead of reading or writing out of bounds.
 #include "bia_internal.h"
 
@@ -11,10 +20,6 @@ namespace bia {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-
-struct ReqCounts {
-  int64_t units, rows;
-};
 
 __device__ inline void request_geometry(const PlanArgs &a, int b, int32_t &q_start,
                                         int32_t &q_len, int32_t &kv_len) {
@@ -29,80 +34,134 @@ __device__ inline void request_geometry(const PlanArgs &a, int b, int32_t &q_sta
   kv_len = pages > 0 ? (pages - 1) * a.page_size + a.kv_last_page_len[b] : 0;
 }
 
-__device__ inline ReqCounts request_counts(const PlanArgs &a, int32_t q_len, int32_t kv_len,
-                                           int32_t &nsp) {
-  ReqCounts c{0, 0};
-  c.units = request_units(q_len, kv_len, a.tile_tokens, a.tiles_per_unit, a.causal, a.split,
-                          &nsp);
-  if (nsp > 1) c.rows = static_cast<int64_t>(q_len) * nsp;
-  return c;
+// Exclusive scan of one value per thread across the block; returns the
+// thread's exclusive prefix and writes the block total to *total.
+template <typename T>
+__device__ T block_exclusive_scan(T v, T *scratch, T *total) {
+  const int tid = threadIdx.x;
+  scratch[tid] = v;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const T x = tid >= off ? scratch[tid - off] : T(0);
+    __syncthreads();
+    scratch[tid] += x;
+    __syncthreads();
+  }
+  const T incl = scratch[tid];
+  *total = scratch[kPlanThreads - 1];
+  __syncthreads();
+  return incl - v;
+}
+
+__device__ inline int find_group_owner(const int32_t *group_off, int batch, int32_t g) {
+  int lo = 0, hi = batch - 1; // largest b with group_off[b] <= g
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (group_off[mid] <= g)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
-  __shared__ int64_t s_units[kPlanThreads];
-  __shared__ int64_t s_rows[kPlanThreads];
+  __shared__ int64_t s_scan[kPlanThreads];
   __shared__ int s_ok;
   const int tid = threadIdx.x;
-  const int per = (a.batch + kPlanThreads - 1) / kPlanThreads;
-  const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
   if (tid == 0) a.status[0] = 0;
 
-  int64_t my_units = 0, my_rows = 0;
+  // ---- A: per request
+  const int per = (a.batch + kPlanThreads - 1) / kPlanThreads;
+  const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
+  int64_t my_groups = 0, my_rows = 0;
   for (int b = lo; b < hi; ++b) {
-    int32_t q_start, q_len, kv_len, nsp;
+    int32_t q_start, q_len, kv_len;
     request_geometry(a, b, q_start, q_len, kv_len);
-    ReqCounts c = request_counts(a, q_len, kv_len, nsp);
-    my_units += c.units;
-    my_rows += c.rows;
+    const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
+    const int32_t nsp = tiles > 0 ? tile_splits(q_len, kv_len, tiles - 1, a.tile_tokens,
+                                                a.causal, a.split) : 1;
+    my_groups += (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+    if (nsp > 1) my_rows += static_cast<int64_t>(q_len) * nsp;
   }
-  s_units[tid] = my_units;
-  s_rows[tid] = my_rows;
-  __syncthreads();
-  // inclusive Hillis-Steele scan over the per-thread sums
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    int64_t u = tid >= off ? s_units[tid - off] : 0;
-    int64_t r = tid >= off ? s_rows[tid - off] : 0;
-    __syncthreads();
-    s_units[tid] += u;
-    s_rows[tid] += r;
-    __syncthreads();
-  }
+  int64_t total_groups, total_rows;
+  int64_t group = block_exclusive_scan<int64_t>(my_groups, s_scan, &total_groups);
+  int64_t row = block_exclusive_scan<int64_t>(my_rows, s_scan, &total_rows);
   if (tid == 0) {
-    s_ok = s_units[kPlanThreads - 1] == a.n_units_expected &&
-           s_rows[kPlanThreads - 1] == a.part_rows_expected;
-    if (!s_ok) atomicOr(a.status, kStatusPlanMismatch);
+    s_ok = total_groups == a.n_groups_expected && total_rows == a.part_rows_expected;
+    if (s_ok) a.group_off[a.batch] = static_cast<int32_t>(total_groups);
   }
-  __syncthreads();
-  if (!s_ok) {
-    for (int64_t i = tid; i < a.n_units_expected; i += kPlanThreads)
-      a.units[i] = Unit{-1, 0, 0, 0};
-    return;
-  }
-  int64_t unit = s_units[tid] - my_units;
-  int64_t row = s_rows[tid] - my_rows;
   for (int b = lo; b < hi; ++b) {
-    int32_t q_start, q_len, kv_len, nsp;
+    int32_t q_start, q_len, kv_len;
     request_geometry(a, b, q_start, q_len, kv_len);
-    ReqCounts c = request_counts(a, q_len, kv_len, nsp);
+    const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
+    const int32_t nsp = tiles > 0 ? tile_splits(q_len, kv_len, tiles - 1, a.tile_tokens,
+                                                a.causal, a.split) : 1;
+    const int64_t rows = nsp > 1 ? static_cast<int64_t>(q_len) * nsp : 0;
     ReqInfo r;
     r.q_start = q_start;
     r.q_len = q_len;
     r.kv_len = kv_len;
     r.nsp = nsp;
-    r.rowbase = c.rows > 0 ? row : -1;
+    r.rowbase = rows > 0 ? row : -1;
     r.page_base = a.kv_indptr[b];
     r.pad = 0;
     a.reqs[b] = r;
-    const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
-    const int32_t groups = (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
-    // last q tiles first: they carry the most keys
-    for (int32_t gi = groups - 1; gi >= 0; --gi) {
+    a.group_off[b] = static_cast<int32_t>(group);
+    group += (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+    row += rows;
+  }
+  __syncthreads();
+  const int32_t n_groups = static_cast<int32_t>(a.n_groups_expected);
+
+  // ---- B: split count of every group (reversed within its request)
+  if (s_ok) {
+    for (int32_t g = tid; g < n_groups; g += kPlanThreads) {
+      const int b = find_group_owner(a.group_off, a.batch, g);
+      const ReqInfo r = a.reqs[b];
+      const int32_t tiles = (r.q_len + a.tile_tokens - 1) / a.tile_tokens;
+      const int32_t groups = (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+      const int32_t gi = groups - 1 - (g - a.group_off[b]);
       const int32_t t0 = gi * a.tiles_per_unit;
       const int32_t nt = min(a.tiles_per_unit, tiles - t0);
-      const int32_t n = tile_splits(q_len, kv_len, t0 + nt - 1, a.tile_tokens, a.causal, a.split);
-      for (int32_t s = 0; s < n; ++s) a.units[unit++] = Unit{b, t0, s, nt};
+      a.group_cnt[g] = tile_splits(r.q_len, r.kv_len, t0 + nt - 1, a.tile_tokens, a.causal,
+                                   a.split);
     }
-    row += c.rows;
+  }
+  __syncthreads();
+
+  // ---- C: exclusive scan of the split counts, in chunks of the block size
+  int64_t carry = 0;
+  for (int32_t base = 0; base < n_groups; base += kPlanThreads) {
+    const int32_t g = base + tid;
+    const int32_t v = (s_ok && g < n_groups) ? a.group_cnt[g] : 0;
+    int64_t chunk_total;
+    const int64_t excl = block_exclusive_scan<int64_t>(v, s_scan, &chunk_total);
+    if (s_ok && g < n_groups) a.group_cnt[g] = static_cast<int32_t>(carry + excl);
+    carry += chunk_total;
+  }
+  if (tid == 0 && s_ok && carry != a.n_units_expected) s_ok = 0;
+  __syncthreads();
+  if (!s_ok) {
+    if (tid == 0) atomicOr(a.status, kStatusPlanMismatch);
+    for (int64_t i = tid; i < a.n_units_expected; i += kPlanThreads)
+      a.units[i] = Unit{-1, 0, 0, 0};
+    return;
+  }
+
+  // ---- D: the units of every group
+  for (int32_t g = tid; g < n_groups; g += kPlanThreads) {
+    const int b = find_group_owner(a.group_off, a.batch, g);
+    const ReqInfo r = a.reqs[b];
+    const int32_t tiles = (r.q_len + a.tile_tokens - 1) / a.tile_tokens;
+    const int32_t groups = (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+    const int32_t gi = groups - 1 - (g - a.group_off[b]);
+    const int32_t t0 = gi * a.tiles_per_unit;
+    const int32_t nt = min(a.tiles_per_unit, tiles - t0);
+    const int32_t n = tile_splits(r.q_len, r.kv_len, t0 + nt - 1, a.tile_tokens, a.causal,
+                                  a.split);
+    int64_t u = a.group_cnt[g];
+    for (int32_t s = 0; s < n; ++s) a.units[u++] = Unit{b, t0, s, nt};
   }
 }
 

@@ -13,11 +13,13 @@
 //                  absolute key position, keeps a running max / sum, writes P
 //                  as bf16 back into the S columns of TMEM (tcgen05.st)
 //   O (+)= P V     tcgen05.mma with A = P read from TMEM, B = V in shared memory
-// Warp roles (12 warps): 0-3 softmax + epilogue of tile A, 4-7 of tile B,
-// 8 issues the MMAs (one thread) and owns TMEM, 9-11 gather K/V rows with
-// cp.async into a two-stage ring.  mbarriers order the roles; the MMA order
-// PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one tile's softmax overlap the
-// other tile's MMAs.
+// Warp roles (10 warps): 0-3 softmax + epilogue of tile A, 4-7 of tile B,
+// 8 issues the MMAs (one thread) and owns TMEM, 9 gathers the q rows and the
+// paged K/V rows with TMA tile::gather4 (each lane fetches four rows per
+// 64-column half; rows past the sequence or on a bad page come from outside
+// the tensor map and read as zeros) into a two-stage ring.  mbarriers order
+// the roles; the MMA order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one
+// tile's softmax overlap the other tile's MMAs.
 //
 // Invariance: every reduction boundary is a function of absolute key
 // positions and the split size.  A row's block sequence is the same in any
@@ -35,9 +37,8 @@ namespace bia {
 namespace {
 
 constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp0 = 9;
-constexpr int kLoadThreads = 96;
-constexpr int kThreads = 384;
+constexpr int kProducerWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kAtom = kTileRows * 128; // one SW128 column block: 128 rows x 64 bf16
 constexpr float kRescaleThreshold = 8.0f; // log2 units
 
@@ -63,9 +64,8 @@ struct TileInfo {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ AttnArgs a) {
   using L = Smem<D>;
-  constexpr int QCH = D / 8; // 16-byte chunks per row
   constexpr uint32_t kIdescS = idesc_bf16(128, kKvBlock, false);
   constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
   constexpr uint32_t kTmemCols = 512;
@@ -105,10 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) 
 
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (tid == 0) {
-    mbar_init(bar(L::kQFull), kLoadThreads);
+    mbar_init(bar(L::kQFull), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kKFull + s), kLoadThreads);
-      mbar_init(bar(L::kVFull + s), kLoadThreads);
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kVFull + s), 1);
       mbar_init(bar(L::kKvEmpty + s), 1);
       mbar_init(bar(L::kSFull + s), 1);
       mbar_init(bar(L::kPFull + s), 4);
@@ -124,60 +124,57 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) 
   auto tS = [&](int t) { return tmem + 128u * t; };
   auto tO = [&](int t) { return tmem + 256u + static_cast<uint32_t>(D) * t; };
 
-  if (warp >= kLoadWarp0) {
-    // ------------------------------------------------------------ loaders
-    const int lt = tid - kLoadWarp0 * 32;
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
     const int page_mask = (1 << a.page_shift) - 1;
+    if (lane == 0) mbar_expect_tx(bar(L::kQFull), 2u * L::kTile);
+    __syncwarp();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const int32_t t0 = ti[t].tile * T;
-      for (int idx = lt; idx < kTileRows * QCH; idx += kLoadThreads) {
-        const int rr = idx / QCH, c = idx % QCH;
-        const int32_t tl = t0 + rr / G;
+      int32_t rows[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = 4 * lane + i;
+        const int32_t tl = ti[t].tile * T + rr / G;
         const bool ok = ti[t].has && tl < r.q_len;
-        const uint16_t *src =
-            ok ? a.q + (static_cast<int64_t>(r.q_start + tl) * a.Hq + kvh * G + rr % G) * D + c * 8
-               : a.q;
-        cp_async16(sQ(t) + (c >> 3) * kAtom + sw128(rr, c & 7), src, ok);
+        rows[i] = ok ? (r.q_start + tl) * a.Hq + kvh * G + rr % G : a.q_rows;
       }
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h)
+        tma_gather4(sQ(t) + h * kAtom + lane * 512, &a.tm_q, 64 * h, rows[0], rows[1], rows[2],
+                    rows[3], bar(L::kQFull));
     }
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_proxy_async();
-    mbar_arrive(bar(L::kQFull));
     for (int j = 0; j < n_blocks; ++j) {
       const int st = j & 1;
       if (j >= 2 && !mbar_wait(bar(L::kKvEmpty + st), ((j >> 1) - 1) & 1, a.status)) break;
-      const int32_t key0 = key_begin + j * kKvBlock;
+      const int32_t key0 = key_begin + j * kKvBlock + 4 * lane;
+      int32_t rows[4];
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint16_t *cache = which == 0 ? a.k_cache : a.v_cache;
-        const uint32_t dst0 = which == 0 ? sK(st) : sV(st);
-        for (int idx = lt; idx < kKvBlock * QCH; idx += kLoadThreads) {
-          const int kr = idx / QCH, c = idx % QCH;
-          const int32_t key = key0 + kr;
-          bool ok = key < r.kv_len;
-          int64_t off = 0;
-          if (ok) {
-            const int32_t page = __ldg(a.kv_indices + r.page_base + (key >> a.page_shift));
-            if (page < 0 || page >= a.num_pages) {
-              atomicOr(a.status, kStatusBadPage);
-              ok = false;
-            } else {
-              off = (((static_cast<int64_t>(page) << a.page_shift) + (key & page_mask)) * a.Hkv +
-                     kvh) * D + c * 8;
-            }
-          }
-          cp_async16(dst0 + (c >> 3) * kAtom + sw128(kr, c & 7), cache + off, ok);
+      for (int i = 0; i < 4; ++i) {
+        const int32_t key = key0 + i;
+        rows[i] = a.kv_rows;
+        if (key < r.kv_len) {
+          const int32_t page = __ldg(a.kv_indices + r.page_base + (key >> a.page_shift));
+          if (page < 0 || page >= a.num_pages)
+            atomicOr(a.status, kStatusBadPage);
+          else
+            rows[i] = ((page << a.page_shift) + (key & page_mask)) * a.Hkv + kvh;
         }
-        cp_async_commit();
       }
-      cp_async_wait_group<1>();
-      fence_proxy_async();
-      mbar_arrive(bar(L::kKFull + st));
-      cp_async_wait_group<0>();
-      fence_proxy_async();
-      mbar_arrive(bar(L::kVFull + st));
+      __syncwarp();
+      if (lane == 0) {
+        mbar_expect_tx(bar(L::kKFull + st), L::kTile);
+        mbar_expect_tx(bar(L::kVFull + st), L::kTile);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h)
+        tma_gather4(sK(st) + h * kAtom + lane * 512, &a.tm_k, 64 * h, rows[0], rows[1], rows[2],
+                    rows[3], bar(L::kKFull + st));
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h)
+        tma_gather4(sV(st) + h * kAtom + lane * 512, &a.tm_v, 64 * h, rows[0], rows[1], rows[2],
+                    rows[3], bar(L::kVFull + st));
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -246,13 +243,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) 
       // pass 1: block max
       float bm = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kKvBlock / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS(t) + lane_base + c * 32, v);
+      for (int c = 0; c < kKvBlock / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(tS(t) + lane_base + c * 16, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c * 32 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v[i]));
+        for (int i = 0; i < 16; ++i)
+          if (c * 16 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v[i]));
       }
       bm = bm == -INFINITY ? -INFINITY : bm * a.scale_log2;
       float m_use = m, alpha = 1.f;
@@ -264,22 +261,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) 
       // pass 2: P = 2^(s*scale - m), row sum, P -> TMEM (bf16, over S)
       float psum = 0.f;
 #pragma unroll
-      for (int c = 0; c < kKvBlock / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS(t) + lane_base + c * 32, v);
+      for (int c = 0; c < kKvBlock / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(tS(t) + lane_base + c * 16, v);
         tmem_wait_ld();
-        uint32_t pk[16];
+        uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = (c * 32 + i < n_vis)
+        for (int i = 0; i < 16; i += 2) {
+          const float p0 = (c * 16 + i < n_vis)
                                ? ex2(fmaf(__uint_as_float(v[i]), a.scale_log2, -m_sub)) : 0.f;
-          const float p1 = (c * 32 + i + 1 < n_vis)
+          const float p1 = (c * 16 + i + 1 < n_vis)
                                ? ex2(fmaf(__uint_as_float(v[i + 1]), a.scale_log2, -m_sub)) : 0.f;
           psum += p0;
           psum += p1;
           pk[i / 2] = pack_bf16(p0, p1);
         }
-        tmem_st16(tS(t) + lane_base + c * 16, pk);
+        tmem_st8(tS(t) + lane_base + c * 8, pk);
       }
       l = fmaf(l, alpha, psum);
       m = m_use;
@@ -287,13 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) 
       // completed: S of this block was issued after it)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO(t) + lane_base + c * 32, v);
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tO(t) + lane_base + c * 16, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tO(t) + lane_base + c * 32, v);
+          for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st16(tO(t) + lane_base + c * 16, v);
         }
       }
       tmem_wait_st();
@@ -313,23 +310,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) 
       const int64_t part_row =
           (r.rowbase + static_cast<int64_t>(t_row) * r.nsp + u.split) * a.Hq + h_row;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
+      for (int c = 0; c < D / 16; ++c) {
+        float o[16];
         if (have_o) {
-          uint32_t v[32];
-          tmem_ld32(tO(t) + lane_base + c * 32, v);
+          uint32_t v[16];
+          tmem_ld16(tO(t) + lane_base + c * 16, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = nonzero ? __fdiv_rn(__uint_as_float(v[i]), l) : 0.f;
+          for (int i = 0; i < 16; ++i) o[i] = nonzero ? __fdiv_rn(__uint_as_float(v[i]), l) : 0.f;
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          for (int i = 0; i < 16; ++i) o[i] = 0.f;
         }
         if (!row_valid) continue;
         if (final_row) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.out + out_row * D + c * 32);
+          uint4 *dst = reinterpret_cast<uint4 *>(a.out + out_row * D + c * 16);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             uint4 w;
             w.x = pack_bf16(o[q * 8 + 0], o[q * 8 + 1]);
             w.y = pack_bf16(o[q * 8 + 2], o[q * 8 + 3]);
@@ -338,9 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const AttnArgs a) 
             dst[q] = w;
           }
         } else {
-          float4 *dst = reinterpret_cast<float4 *>(a.part_o + part_row * D + c * 32);
+          float4 *dst = reinterpret_cast<float4 *>(a.part_o + part_row * D + c * 16);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
+          for (int q = 0; q < 4; ++q)
             dst[q] = make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
         }
       }
