@@ -135,6 +135,35 @@ BIA_API size_t bia_decode_workspace_size(const bia_attn_desc *desc, const int32_
                                  const int32_t *kv_last_page_len_host, int32_t batch,
                                  int32_t split_size);
 
+/* Size of the library-owned scratch array behind bia_decode_paged_noalloc. */
+#define BIA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * bia_decode_paged without a workspace argument, for callers that cannot
+ * allocate device memory: plugin / extension hooks of inference engines whose
+ * enqueue step may not call cudaMalloc (it can synchronise the device, break
+ * a CUDA-graph capture in progress or exceed a memory budget fixed up front),
+ * and hosts that account for all device memory before serving.  There is no
+ * counterpart on the pages; it is a packaging of the same decode path.
+ *
+ * Arguments, layouts and results are those of bia_decode_paged.  The scratch
+ * space lives in a statically sized __device__ array of
+ * BIA_DECODE_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds
+ * until the process exits; a call whose bia_decode_workspace_size exceeds it
+ * returns BIA_ERR_WORKSPACE_TOO_SMALL without enqueuing anything.  Nothing is
+ * allocated (no cudaMalloc / cudaFree).  The first call on each device looks
+ * up the array's device address with that device current; make that first
+ * call before any stream capture.  All calls share the one array, which keeps
+ * the previous call's contents (every call rewrites what it reads), so calls
+ * whose work overlaps on the GPU - different streams, or different host
+ * threads - race and must be serialised by the caller.
+ */
+BIA_API int bia_decode_paged_noalloc(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                             const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
+                             const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                             const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                             int32_t batch, int32_t split_size, void *out, float *lse,
+                             void *stream);
 
 /*
  * Fixed-order log-sum-exp merge of attention states (the merge the split-KV

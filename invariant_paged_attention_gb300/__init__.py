@@ -32,7 +32,7 @@ BIA_DECODE_SPLIT = 2048
 EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged",
            "bia_decode_workspace_size", "bia_merge_states", "bia_q_tile_tokens",
            "bia_status_string", "bia_read_status", "bia_set_profile_events",
-           "bia_launch_count", "bia_last_error")
+           "bia_launch_count", "bia_last_error", "bia_decode_paged_noalloc")
 
 
 class BiaError(RuntimeError):
@@ -88,6 +88,9 @@ def load(path: str = LIB_PATH):
     lib.bia_launch_count.restype = ctypes.c_uint64
     lib.bia_last_error.argtypes = []
     lib.bia_last_error.restype = ctypes.c_char_p
+    lib.bia_decode_paged_noalloc.argtypes = [dp, vp, vp, vp, i64, vp, vp, vp, vp, vp, i32, i32,
+                                             vp, vp, vp]
+    lib.bia_decode_paged_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -163,6 +166,24 @@ def bia_decode_paged(desc, q, k_cache, v_cache, kv_indptr, kv_indices, kv_last_p
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
     if rc != BIA_OK:
         raise BiaError(rc, "bia_decode_paged")
+
+
+BIA_DECODE_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def bia_decode_paged_noalloc(desc, q, k_cache, v_cache, kv_indptr, kv_indices, kv_last_page_len,
+                             kv_indptr_host, kv_last_page_len_host, out, lse=None, split_size=0,
+                             stream=None):
+    """bia_decode_paged for callers that cannot allocate device memory: no
+    workspace argument; the library's static scratch array is used instead
+    (see include/bia.h for its size, first-call and concurrency rules)."""
+    kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
+    rc = load().bia_decode_paged_noalloc(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(kvp), _ptr(last),
+        len(kvp) - 1, int(split_size), _ptr(out), _ptr(lse), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_decode_paged_noalloc")
 
 
 def bia_merge_states(v, s, out, out_lse=None, num_states=None, stream=None):
