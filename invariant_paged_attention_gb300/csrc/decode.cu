@@ -81,6 +81,22 @@ __device__ __forceinline__ void group_reduce(float (&s)[G]) {
   }
 }
 
+// G == 4, 16 lanes per key: sums the four partial scores over the key's 16
+// lanes and leaves head (sub >> 2)'s total on lanes 4h..4h+3 of the group
+// (identical bits on the four).
+__device__ __forceinline__ float reduce_scatter4(const float (&s)[4]) {
+  const int sub = threadIdx.x & 15;
+  const bool b3 = (sub >> 3) & 1, b2 = (sub >> 2) & 1;
+  const float kx = b3 ? s[2] : s[0], ky = b3 ? s[3] : s[1];
+  const float sx = b3 ? s[0] : s[2], sy = b3 ? s[1] : s[3];
+  const float px = kx + __shfl_xor_sync(0xffffffffu, sx, 8);
+  const float py = ky + __shfl_xor_sync(0xffffffffu, sy, 8);
+  float c = (b2 ? py : px) + __shfl_xor_sync(0xffffffffu, b2 ? px : py, 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     decode_kernel(const AttnArgs a) {
@@ -89,6 +105,10 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
   constexpr int KPW = 32 / LPK;      // key rows per warp step
   constexpr int STEPS = kChunk / KPW; // steps per chunk
   constexpr int NS = L::kStages;
+  // G == 4 with 16 lanes per key: the softmax state of head sub/4 lives on
+  // lanes 4h..4h+3 of each lane group (m[0], l[0]); otherwise every lane keeps
+  // all G states
+  constexpr bool kOwnHead = (G == 4 && LPK == 16);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -202,28 +222,60 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
         f32x2_split(acc, x, y);
         sc[g] = x + y;
       }
-      group_reduce<G, LPK>(sc);
-      if (key0 + kl >= key_end) continue; // past the split's last key
+      const bool valid = key0 + kl < key_end; // past the split's last key: no weight
       const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
                               bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
-      // online softmax with lazy rescale: the running max moves only when a
-      // score exceeds it by more than 2^8 (a function of this lane group's own
-      // keys, so the result is the same in any batch)
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (sc[g] > m[g] + kLazyThreshold || m[g] == -INFINITY) {
-          const float alpha = ex2(m[g] - sc[g]);
-          l[g] *= alpha;
-          const uint64_t a2 = f32x2(alpha, alpha);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
-          m[g] = sc[g];
+      if constexpr (kOwnHead) {
+        // each lane runs the online softmax of head sub/4 only; the weights of
+        // the four heads are then gathered for P.V
+        const float c = reduce_scatter4(sc);
+        const bool resc = valid && (c > m[0] + kLazyThreshold || m[0] == -INFINITY);
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2(m[0] - c);
+          l[0] *= alpha;
+          m[0] = c;
         }
-        const float p = ex2(sc[g] - m[g]);
-        l[g] += p;
-        const uint64_t p2 = f32x2(p, p);
+        const float p = valid ? ex2(c - m[0]) : 0.f;
+        l[0] += p;
+        const int base = lane & ~15;
+        if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
+          for (int g = 0; g < G; ++g) {
+            const float ag = __shfl_sync(0xffffffffu, alpha, base + 4 * g);
+            const uint64_t a2 = f32x2(ag, ag);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pg = __shfl_sync(0xffffffffu, p, base + 4 * g);
+          const uint64_t p2 = f32x2(pg, pg);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
+        }
+      } else {
+        group_reduce<G, LPK>(sc);
+        // online softmax with lazy rescale: the running max moves only when a
+        // score exceeds it by more than 2^8 (a function of this lane group's
+        // own keys, so the result is the same in any batch)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          if (valid && (sc[g] > m[g] + kLazyThreshold || m[g] == -INFINITY)) {
+            const float alpha = ex2(m[g] - sc[g]);
+            l[g] *= alpha;
+            const uint64_t a2 = f32x2(alpha, alpha);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
+            m[g] = sc[g];
+          }
+          const float p = valid ? ex2(sc[g] - m[g]) : 0.f;
+          l[g] += p;
+          const uint64_t p2 = f32x2(p, p);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
+        }
       }
     }
     __syncwarp();
@@ -231,6 +283,15 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     if (i + NS < my_chunks) issue(i + NS);
   }
 
+  if constexpr (kOwnHead) {
+    const int base = lane & ~15;
+    const float m_own = m[0], l_own = l[0];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = __shfl_sync(0xffffffffu, m_own, base + 4 * g);
+      l[g] = __shfl_sync(0xffffffffu, l_own, base + 4 * g);
+    }
+  }
   float o[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g)

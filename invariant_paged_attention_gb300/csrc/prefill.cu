@@ -49,8 +49,8 @@ struct Smem {
   static constexpr int kKV = 2 * kTile;              // stage s: K at kKV + 2s*kTile, V after it
   static constexpr int kBar = 6 * kTile;
   // barriers (8 bytes each)
-  static constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kKvEmpty = 5, kSFull = 7,
-                       kPFull = 9, kODone = 11, kNumBars = 13;
+  static constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kKEmpty = 5, kVEmpty = 7,
+                       kSFull = 9, kPFull = 11, kODone = 13, kNumBars = 15;
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kBytes = kSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kVFull + s), 1);
-      mbar_init(bar(L::kKvEmpty + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
       mbar_init(bar(L::kSFull + s), 1);
       mbar_init(bar(L::kPFull + s), 4);
       mbar_init(bar(L::kODone + s), 1);
@@ -144,33 +145,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tma_gather4(sQ(t) + h * kAtom + lane * 512, &a.tm_q, 64 * h, rows[0], rows[1], rows[2],
                     rows[3], bar(L::kQFull));
     }
+    // page indices of this lane's four keys of block j (one block ahead)
+    auto fetch = [&](int j, int32_t (&pg)[4]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int32_t key = key_begin + j * kKvBlock + 4 * lane + i;
+        pg[i] = (j < n_blocks && key < r.kv_len)
+                    ? __ldg(a.kv_indices + r.page_base + (key >> a.page_shift)) : -1;
+      }
+    };
+    int32_t pg[4];
+    fetch(0, pg);
     for (int j = 0; j < n_blocks; ++j) {
       const int st = j & 1;
-      if (j >= 2 && !mbar_wait(bar(L::kKvEmpty + st), ((j >> 1) - 1) & 1, a.status)) break;
-      const int32_t key0 = key_begin + j * kKvBlock + 4 * lane;
       int32_t rows[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int32_t key = key0 + i;
-        rows[i] = a.kv_rows;
+        const int32_t key = key_begin + j * kKvBlock + 4 * lane + i;
+        rows[i] = a.kv_rows; // outside the map: zeros
         if (key < r.kv_len) {
-          const int32_t page = __ldg(a.kv_indices + r.page_base + (key >> a.page_shift));
-          if (page < 0 || page >= a.num_pages)
+          if (pg[i] < 0 || pg[i] >= a.num_pages)
             atomicOr(a.status, kStatusBadPage);
           else
-            rows[i] = ((page << a.page_shift) + (key & page_mask)) * a.Hkv + kvh;
+            rows[i] = ((pg[i] << a.page_shift) + (key & page_mask)) * a.Hkv + kvh;
         }
       }
+      fetch(j + 1, pg); // in flight while this block's copies are issued
+      bool ok = j < 2 || mbar_wait(bar(L::kKEmpty + st), ((j >> 1) - 1) & 1, a.status);
+      if (!ok) break;
       __syncwarp();
-      if (lane == 0) {
-        mbar_expect_tx(bar(L::kKFull + st), L::kTile);
-        mbar_expect_tx(bar(L::kVFull + st), L::kTile);
-      }
+      if (lane == 0) mbar_expect_tx(bar(L::kKFull + st), L::kTile);
       __syncwarp();
 #pragma unroll
       for (int h = 0; h < D / 64; ++h)
         tma_gather4(sK(st) + h * kAtom + lane * 512, &a.tm_k, 64 * h, rows[0], rows[1], rows[2],
                     rows[3], bar(L::kKFull + st));
+      ok = j < 2 || mbar_wait(bar(L::kVEmpty + st), ((j >> 1) - 1) & 1, a.status);
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_expect_tx(bar(L::kVFull + st), L::kTile);
+      __syncwarp();
 #pragma unroll
       for (int h = 0; h < D / 64; ++h)
         tma_gather4(sV(st) + h * kAtom + lane * 512, &a.tm_v, 64 * h, rows[0], rows[1], rows[2],
@@ -207,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int nb0 = ti[0].n_blocks, nb1 = ti[1].n_blocks;
       if (nb0 > 0) issue_s(0, 0);
       if (nb1 > 0) issue_s(1, 0);
+      if (ok && n_blocks > 0) mma_commit(bar(L::kKEmpty + 0)); // K_0 read by both S(0)
       for (int j = 0; j < n_blocks && ok; ++j) {
         const int st = j & 1;
         ok = mbar_wait(bar(L::kVFull + st), (j >> 1) & 1, a.status);
@@ -215,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (j + 1 < nb0) issue_s(0, j + 1);
         if (j < nb1) issue_pv(1, j, nb1);
         if (j + 1 < nb1) issue_s(1, j + 1);
-        mma_commit(bar(L::kKvEmpty + st));
+        if (!ok) break;
+        mma_commit(bar(L::kVEmpty + st));                                // V_j read
+        if (j + 1 < n_blocks) mma_commit(bar(L::kKEmpty + ((j + 1) & 1))); // K_{j+1} read
       }
     }
     __syncwarp();
@@ -240,16 +257,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tc_fence_after();
       const int32_t key0 = key_begin + j * kKvBlock;
       const int32_t n_vis = vis_last - key0 + 1; // visible columns of this block
-      // pass 1: block max
+      // blocks every row of the warp sees in full skip the per-column mask
+      const bool full = __all_sync(0xffffffffu, n_vis >= kKvBlock);
+      // pass 1: block max of the raw scores
       float bm = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kKvBlock / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tS(t) + lane_base + c * 16, v);
+      for (int c = 0; c < kKvBlock / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS(t) + lane_base + c * 32, v);
         tmem_wait_ld();
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (c * 16 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v[i]));
+          for (int i = 0; i < 32; i += 2)
+            bm = fmax3(bm, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v[i]));
+        }
       }
       bm = bm == -INFINITY ? -INFINITY : bm * a.scale_log2;
       float m_use = m, alpha = 1.f;
@@ -258,8 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         alpha = ex2(m - bm); // 0 when m == -inf
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      // pass 2: P = 2^(s*scale - m), row sum, P -> TMEM (bf16, over S)
-      float psum = 0.f;
+      // pass 2: P = 2^(s*scale - m) on fp32 pairs, row sum, P -> TMEM (bf16, over S)
+      const uint64_t scale2 = f32x2(a.scale_log2, a.scale_log2);
+      const uint64_t neg2 = f32x2(-m_sub, -m_sub);
+      uint64_t psum2 = 0;
 #pragma unroll
       for (int c = 0; c < kKvBlock / 16; ++c) {
         uint32_t v[16];
@@ -268,16 +295,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-          const float p0 = (c * 16 + i < n_vis)
-                               ? ex2(fmaf(__uint_as_float(v[i]), a.scale_log2, -m_sub)) : 0.f;
-          const float p1 = (c * 16 + i + 1 < n_vis)
-                               ? ex2(fmaf(__uint_as_float(v[i + 1]), a.scale_log2, -m_sub)) : 0.f;
-          psum += p0;
-          psum += p1;
+          float x0, x1;
+          f32x2_split(ffma2r(f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), scale2,
+                             neg2),
+                      x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
+          if (!full) {
+            if (c * 16 + i >= n_vis) p0 = 0.f;
+            if (c * 16 + i + 1 >= n_vis) p1 = 0.f;
+          }
+          psum2 = fadd2(psum2, f32x2(p0, p1));
           pk[i / 2] = pack_bf16(p0, p1);
         }
         tmem_st8(tS(t) + lane_base + c * 8, pk);
       }
+      float ps0, ps1;
+      f32x2_split(psum2, ps0, ps1);
+      const float psum = ps0 + ps1;
       l = fmaf(l, alpha, psum);
       m = m_use;
       // rescale the running O row when the max moved (the previous P.V has
