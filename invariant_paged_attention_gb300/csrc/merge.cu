@@ -61,14 +61,16 @@ __device__ __forceinline__ int owner(const int32_t *qo_indptr, int batch, int64_
 }
 
 // Merge of the split partials a prefill / decode call left in the workspace:
-// one warp per q token, looping over its q heads.  Rows whose q tile had a
-// single split were written by the attention kernel and are skipped.
+// one CTA per q token, its q heads spread over the warps.  A warp folds one
+// row: lane s first loads the LSE of split s (all splits in flight at once),
+// then the states are folded in ascending split order.  Rows whose q tile had
+// a single split were written by the attention kernel and are skipped.
 template <int V>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_partials_kernel(const AttnArgs a) {
   const int D = a.D;
-  const int lane = threadIdx.x & 31;
-  const int64_t token = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t token = blockIdx.x;
   if (token >= a.total_rows) return;
   const int b = a.qo_indptr ? owner(a.qo_indptr, a.batch, token) : static_cast<int>(token);
   const ReqInfo r = a.reqs[b];
@@ -79,18 +81,23 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const int32_t p = a.causal ? r.kv_len - r.q_len + t : r.kv_len - 1;
   const int32_t n_row = min(n_tile, p / a.split + 1);
   const int64_t base = (r.rowbase + static_cast<int64_t>(t) * r.nsp) * a.Hq;
-  for (int h = 0; h < a.Hq; ++h) {
+  for (int h = warp; h < a.Hq; h += kMergeWarps) {
     float L = -INFINITY;
     float o[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) o[i] = 0.f;
-    for (int s = 0; s < n_row; ++s) {
-      const int64_t idx = base + static_cast<int64_t>(s) * a.Hq + h;
-      const float ls = __ldg(a.part_lse + idx);
-      if (ls == -INFINITY) continue;
-      float v[V];
-      load_state<V>(a.part_o + idx * D, D, lane, v);
-      fold_state<V>(L, o, ls, v);
+    for (int s0 = 0; s0 < n_row; s0 += 32) {
+      const int n_here = min(32, n_row - s0);
+      const float ls_lane = lane < n_here
+          ? __ldg(a.part_lse + base + static_cast<int64_t>(s0 + lane) * a.Hq + h) : -INFINITY;
+      for (int k = 0; k < n_here; ++k) {
+        const float ls = __shfl_sync(0xffffffffu, ls_lane, k);
+        if (ls == -INFINITY) continue;
+        const int64_t idx = base + static_cast<int64_t>(s0 + k) * a.Hq + h;
+        float v[V];
+        load_state<V>(a.part_o + idx * D, D, lane, v);
+        fold_state<V>(L, o, ls, v);
+      }
     }
     if (L == -INFINITY) {
 #pragma unroll
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t st) {
   if (a.total_rows == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((a.total_rows + kMergeWarps - 1) / kMergeWarps);
+  const unsigned grid = static_cast<unsigned>(a.total_rows);
   merge_partials_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(a);
   return cudaGetLastError();
 }

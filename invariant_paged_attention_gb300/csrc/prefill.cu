@@ -63,6 +63,69 @@ struct TileInfo {
   bool has;           // the tile exists and touches this split
 };
 
+// Max of this thread's row of S (128 fp32 columns at taddr), over the first
+// n_vis columns unless FULL.  Two batches of 64 columns: two loads, one wait.
+template <bool FULL>
+__device__ __forceinline__ float row_block_max(uint32_t taddr, int32_t n_vis) {
+  float bm = -INFINITY;
+#pragma unroll
+  for (int h = 0; h < kKvBlock / 64; ++h) {
+    uint32_t v0[32], v1[32];
+    tmem_ld32(taddr + h * 64, v0);
+    tmem_ld32(taddr + h * 64 + 32, v1);
+    tmem_wait_ld();
+    if constexpr (FULL) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        bm = fmax3(bm, __uint_as_float(v0[i]), __uint_as_float(v0[i + 1]));
+        bm = fmax3(bm, __uint_as_float(v1[i]), __uint_as_float(v1[i + 1]));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (h * 64 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v0[i]));
+        if (h * 64 + 32 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v1[i]));
+      }
+    }
+  }
+  return bm;
+}
+
+// P = 2^(s*scale - m_sub) of this thread's row (zero past n_vis unless FULL),
+// written as bf16 pairs over the first 64 columns of the same TMEM row;
+// returns the row sum of the fp32 P.
+template <bool FULL>
+__device__ __forceinline__ float row_block_p(uint32_t taddr, int32_t n_vis, float scale,
+                                             float m_sub) {
+  const uint64_t scale2 = f32x2(scale, scale);
+  const uint64_t neg2 = f32x2(-m_sub, -m_sub);
+  uint64_t psum2 = 0;
+#pragma unroll
+  for (int c = 0; c < kKvBlock / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+    tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float x0, x1;
+      f32x2_split(ffma2r(f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), scale2, neg2),
+                  x0, x1);
+      float p0 = ex2(x0), p1 = ex2(x1);
+      if constexpr (!FULL) {
+        if (c * 32 + i >= n_vis) p0 = 0.f;
+        if (c * 32 + i + 1 >= n_vis) p1 = 0.f;
+      }
+      psum2 = fadd2(psum2, f32x2(p0, p1));
+      pk[i / 2] = pack_bf16(p0, p1);
+    }
+    tmem_st16(taddr + c * 16, pk);
+  }
+  float ps0, ps1;
+  f32x2_split(psum2, ps0, ps1);
+  return ps0 + ps1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ AttnArgs a) {
   using L = Smem<D>;
@@ -259,23 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int32_t n_vis = vis_last - key0 + 1; // visible columns of this block
       // blocks every row of the warp sees in full skip the per-column mask
       const bool full = __all_sync(0xffffffffu, n_vis >= kKvBlock);
-      // pass 1: block max of the raw scores
-      float bm = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kKvBlock / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS(t) + lane_base + c * 32, v);
-        tmem_wait_ld();
-        if (full) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            bm = fmax3(bm, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v[i]));
-        }
-      }
+      const uint32_t srow = tS(t) + lane_base;
+      float bm = full ? row_block_max<true>(srow, n_vis) : row_block_max<false>(srow, n_vis);
       bm = bm == -INFINITY ? -INFINITY : bm * a.scale_log2;
       float m_use = m, alpha = 1.f;
       if (bm > m + kRescaleThreshold || (m == -INFINITY && bm != -INFINITY)) {
@@ -283,35 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         alpha = ex2(m - bm); // 0 when m == -inf
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      // pass 2: P = 2^(s*scale - m) on fp32 pairs, row sum, P -> TMEM (bf16, over S)
-      const uint64_t scale2 = f32x2(a.scale_log2, a.scale_log2);
-      const uint64_t neg2 = f32x2(-m_sub, -m_sub);
-      uint64_t psum2 = 0;
-#pragma unroll
-      for (int c = 0; c < kKvBlock / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tS(t) + lane_base + c * 16, v);
-        tmem_wait_ld();
-        uint32_t pk[8];
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          float x0, x1;
-          f32x2_split(ffma2r(f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), scale2,
-                             neg2),
-                      x0, x1);
-          float p0 = ex2(x0), p1 = ex2(x1);
-          if (!full) {
-            if (c * 16 + i >= n_vis) p0 = 0.f;
-            if (c * 16 + i + 1 >= n_vis) p1 = 0.f;
-          }
-          psum2 = fadd2(psum2, f32x2(p0, p1));
-          pk[i / 2] = pack_bf16(p0, p1);
-        }
-        tmem_st8(tS(t) + lane_base + c * 8, pk);
-      }
-      float ps0, ps1;
-      f32x2_split(psum2, ps0, ps1);
-      const float psum = ps0 + ps1;
+      const float psum = full ? row_block_p<true>(srow, n_vis, a.scale_log2, m_sub)
+                              : row_block_p<false>(srow, n_vis, a.scale_log2, m_sub);
       l = fmaf(l, alpha, psum);
       m = m_use;
       // rescale the running O row when the max moved (the previous P.V has
@@ -339,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tc_fence_after();
       const bool nonzero = have_o && l > 0.f;
       const float lse = nonzero ? __fmul_rn(__fadd_rn(m, lg2(l)), kLn2) : -INFINITY;
+      const float inv_l = nonzero ? __frcp_rn(l) : 0.f; // o_s = O * (1/l)
       const bool final_row = me.n_splits == 1;
       const int64_t out_row = static_cast<int64_t>(r.q_start + t_row) * a.Hq + h_row;
       const int64_t part_row =
@@ -351,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           tmem_ld16(tO(t) + lane_base + c * 16, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = nonzero ? __fdiv_rn(__uint_as_float(v[i]), l) : 0.f;
+          for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(__uint_as_float(v[i]), inv_l);
         } else {
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] = 0.f;
