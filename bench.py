@@ -435,10 +435,9 @@ def main():
     peaks, peak_kind = load_peaks()
     pk_achieved = flops / pk_avg / 1e12 if prefill else 0.0
     dk_achieved = dbytes / dk_avg / 1e9 if decode else 0.0
-    pre_src = ["invariant_paged_attention_gb300/csrc/prefill.cu",
-               "invariant_paged_attention_gb300/csrc/ptx.cuh"]
-    dec_src = ["invariant_paged_attention_gb300/csrc/decode.cu",
-               "invariant_paged_attention_gb300/csrc/ptx.cuh"]
+    # counters are keyed by the kernel's own translation unit
+    pre_src = ["invariant_paged_attention_gb300/csrc/prefill.cu"]
+    dec_src = ["invariant_paged_attention_gb300/csrc/decode.cu"]
     roofline = {"bound": "tensor", "kernel": "prefill_kernel<128>", "achieved": pk_achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": pk_achieved / peaks["bf16_tflops"],
