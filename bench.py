@@ -58,6 +58,8 @@ def parse_args():
                    help="run one of the two calls (profiling captures of a small case)")
     p.add_argument("--decode-batch", type=int, default=256,
                    help="decode requests (the decode sweep's largest batch by default)")
+    p.add_argument("--sweep", action="store_true",
+                   help="time every workload (one JSON line each) instead of the default step")
     return p.parse_args()
 
 
@@ -100,6 +102,20 @@ def prefill_flops(call: wl.Call, D: int, Hq: int) -> int:
 
 def kv_bytes(call: wl.Call, Hkv: int, D: int) -> int:
     return sum(call.kv_lens) * Hkv * D * 2 * 2
+
+
+def aggregate_over_ranks(local_seconds, units_per_rank, steps, dist=None, device="cpu"):
+    """Whole-job throughput of N replicas: every rank contributes its summed
+    times, the slowest rank's time is the job's time (max over ranks), and the
+    job's work is the sum over ranks.  Returns (units per second, max seconds
+    per item of local_seconds)."""
+    t = torch.tensor(list(local_seconds), dtype=torch.float64, device=device)
+    w = torch.tensor([float(units_per_rank)], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized():
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    tmax = t.tolist()
+    return (w.item() * steps / tmax[0] if tmax[0] > 0 else 0.0), tmax
 
 
 def source_hash(*files) -> str:
@@ -257,10 +273,143 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- our arm
+def run_sweep(args):
+    """One JSON line per workload: each call timed with CUDA events on its
+    stream (median of --steps after --warmup), kernel time from the library's
+    profile events.  For tables; not the driver's single-line contract."""
+    import invariant_paged_attention_gb300 as bia
+    from invariant_paged_attention_gb300 import build as bia_build
+    bia_build.build()
+    bia.load()
+    dev = "cuda:0"
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    peaks, peak_kind = load_peaks()
+
+    def dev_idx(call):
+        return [call.qo_indptr.to(dev), call.kv_indptr.to(dev), call.kv_indices.to(dev),
+                call.kv_last_page_len.to(dev)]
+
+    def time_calls(fns):
+        for _ in range(args.warmup):
+            for f in fns:
+                f(None)
+        call_ms, kern_ms = [], []
+        for _ in range(args.steps):
+            a0, a1, k0, k1 = ev(), ev(), ev(), ev()
+            a0.record(stream)
+            for f in fns:
+                f((k0, k1) if len(fns) == 1 else None)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            call_ms.append(a0.elapsed_time(a1))
+            if len(fns) == 1:
+                kern_ms.append(k0.elapsed_time(k1))
+        bia.bia_set_profile_events(None, None)
+        return statistics.median(call_ms), (statistics.median(kern_ms) if kern_ms else None)
+
+    def prefill_fn(store, call):
+        st = store
+        desc = bia.make_desc(st.num_qo_heads, st.num_kv_heads, st.head_dim, st.page_size)
+        qo, kvp, idx, last = dev_idx(call)
+        ws = torch.empty(bia.bia_prefill_workspace_size(desc, call.qo_indptr, call.kv_indptr,
+                                                        call.kv_last_page_len),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(call.q)
+        lse = torch.empty(call.total_q, st.num_qo_heads, dtype=torch.float32, device=dev)
+
+        def f(evs):
+            if evs:
+                bia.bia_set_profile_events(*evs)
+            bia.bia_prefill_paged(desc, call.q, st.k_cache, st.v_cache, qo, kvp, idx, last,
+                                  call.qo_indptr, call.kv_indptr, call.kv_last_page_len, ws, out,
+                                  lse, stream=stream)
+            if evs:
+                bia.bia_set_profile_events(None, None)
+        return f
+
+    def decode_fn(store, call):
+        st = store
+        desc = bia.make_desc(st.num_qo_heads, st.num_kv_heads, st.head_dim, st.page_size)
+        _, kvp, idx, last = dev_idx(call)
+        ws = torch.empty(bia.bia_decode_workspace_size(desc, call.kv_indptr,
+                                                       call.kv_last_page_len),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(call.q)
+        lse = torch.empty(call.total_q, st.num_qo_heads, dtype=torch.float32, device=dev)
+
+        def f(evs):
+            if evs:
+                bia.bia_set_profile_events(*evs)
+            bia.bia_decode_paged(desc, call.q, st.k_cache, st.v_cache, kvp, idx, last,
+                                 call.kv_indptr, call.kv_last_page_len, ws, out, lse,
+                                 stream=stream)
+            if evs:
+                bia.bia_set_profile_events(None, None)
+        return f
+
+    def emit(name, kind, work, call_ms, kern_ms, extra=None):
+        if kind == "prefill":
+            v, u, pk = work / call_ms / 1e9, "TFLOP/s", peaks["bf16_tflops"]
+            kv = work / kern_ms / 1e9 if kern_ms else None
+        else:
+            v, u, pk = work / call_ms / 1e6, "GB/s", peaks["hbm_gbs"]
+            kv = work / kern_ms / 1e6 if kern_ms else None
+        line = {"workload": name, "kind": kind, "value": v, "unit": u, "call_ms": call_ms,
+                "kernel_ms": kern_ms, "kernel_value": kv,
+                "frac_of_peak": (kv / pk) if kv else None, "peak": pk,
+                "peak_source": peak_kind, "work": work}
+        line.update(extra or {})
+        print(json.dumps(line), flush=True)
+
+    D, Hq, Hkv = 128, 32, 8
+    # prefill workloads
+    st = wl.cfg1_tiny(dev)
+    c = wl.whole_prefill(st)
+    cm, km = time_calls([prefill_fn(st, c)])
+    emit("cfg1 tiny prefill (256 tok, 4q/1kv, d64, page 16)", "prefill",
+         prefill_flops(c, 64, 4), cm, km)
+    st = wl.cfg2_prefill(dev)
+    c = wl.whole_prefill(st)
+    cm, km = time_calls([prefill_fn(st, c)])
+    emit("cfg2 batched prefill (8 req, U[512,8192])", "prefill", prefill_flops(c, D, Hq), cm, km)
+    del st, c
+    st = wl.cfg3_prefix(dev)
+    whole = wl.whole_prefill(st)
+    cm, km = time_calls([prefill_fn(st, whole)])
+    fl = prefill_flops(whole, D, Hq)
+    emit("cfg3 prefix extend, unchunked (4 x 16384 new)", "prefill", fl, cm, km)
+    fns = [prefill_fn(st, cc) for cc in wl.chunked_calls(st, 256)]
+    cm, _ = time_calls(fns)
+    emit("cfg3 prefix extend, 64 chunks of 256", "prefill", fl, cm, None)
+    del st, whole, fns
+    pst, dst = wl.cfg5_mixed(dev)
+    pc = wl.whole_prefill(pst)
+    cm, km = time_calls([prefill_fn(pst, pc)])
+    emit("cfg5 mixed prefill call (4096-tok chunk + 64 one-token extends, page 16)", "prefill",
+         prefill_flops(pc, D, Hq), cm, km, {"kv_bytes": kv_bytes(pc, Hkv, D)})
+    dc = wl.whole_prefill(dst)
+    cm, km = time_calls([decode_fn(dst, dc)])
+    emit("cfg5 decodes (32 x 131072 ctx, page 16)", "decode", kv_bytes(dc, Hkv, D), cm, km)
+    del pst, dst, pc, dc
+    torch.cuda.empty_cache()
+    for B in (1, 8, 64, 256):
+        st = wl.cfg4_decode(dev, B)
+        c = wl.whole_prefill(st)
+        cm, km = time_calls([decode_fn(st, c)])
+        emit(f"cfg4 decode B={B} (ctx U[1024,32768], page 1)", "decode", kv_bytes(c, Hkv, D), cm,
+             km)
+        del st, c
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
 
     import invariant_paged_attention_gb300 as bia
@@ -373,13 +522,11 @@ def main():
     dec_ms = [e_step[i][1].elapsed_time(e_step[i][2]) for i in timed]
     pk_ms = [e_pk[i][0].elapsed_time(e_pk[i][1]) if prefill else 0.0 for i in timed]
     dk_ms = [e_dk[i][0].elapsed_time(e_dk[i][1]) if decode else 0.0 for i in timed]
-    tot = torch.tensor([sum(pre_ms), sum(dec_ms), sum(pk_ms), sum(dk_ms)], dtype=torch.float64,
-                       device=dev)
-    if dist:
-        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-    pre_s, dec_s, pk_s, dk_s = (x / 1000.0 for x in tot.tolist())
     K = args.steps
-    value = world * flops * K / pre_s / 1e12 if prefill else None
+    local = [sum(pre_ms) / 1000.0, sum(dec_ms) / 1000.0, sum(pk_ms) / 1000.0,
+             sum(dk_ms) / 1000.0]
+    flops_rate, (pre_s, dec_s, pk_s, dk_s) = aggregate_over_ranks(local, flops, K, dist, dev)
+    value = flops_rate / 1e12 if prefill else None
     dec_gbs = world * dbytes * K / dec_s / 1e9 if decode else None
     pk_avg, dk_avg = pk_s / K, dk_s / K
 
