@@ -162,3 +162,38 @@ def merge_states(v, lse, num_states=None):
     if rc != 0:
         raise ValueError(f"oracle_merge_states failed with {rc}")
     return out[:n], lo[:n]
+
+
+def append_paged_kv(k_cache, v_cache, k_new, v_new, append_indptr, kv_indptr, kv_indices,
+                    kv_last_page_len, *, page_size):
+    """Paged-KV append, by its definition: the write that puts a chunk's K/V
+    into the cache before that chunk attends to it ("sglang PR #43612",
+    Summary: a chunked prefill reads a cache that already holds the chunk; the
+    pages leave the write itself implicit).  Reading: request b's page table
+    already spans its n_new new tokens as its LAST n_new keys (the same
+    convention as the q tokens of a prefill call), so new token t of request b
+    lands at position p = kv_len - n_new + (t - append_indptr[b]), i.e. page
+    kv_indices[kv_indptr[b] + p // page_size], slot p % page_size, all kv
+    heads.  Returns updated copies of the caches (uint16 bf16 bit patterns,
+    [num_pages, page_size, Hkv, D]); the inputs are left as they are.
+    Raises ValueError on a page index outside the cache or n_new > kv_len."""
+    kc = np.array(_u16(k_cache), copy=True)
+    vc = np.array(_u16(v_cache), copy=True)
+    kn, vn = _u16(k_new), _u16(v_new)
+    ap, kvp = _i32(append_indptr), _i32(kv_indptr)
+    idx, last = _i32(kv_indices), _i32(kv_last_page_len)
+    num_pages = kc.shape[0]
+    for b in range(len(ap) - 1):
+        n_new = int(ap[b + 1] - ap[b])
+        n_pages = int(kvp[b + 1] - kvp[b])
+        kv_len = (n_pages - 1) * page_size + int(last[b]) if n_pages > 0 else 0
+        if n_new > kv_len:
+            raise ValueError(f"request {b}: {n_new} new tokens but only {kv_len} keys")
+        for i in range(n_new):
+            p = kv_len - n_new + i
+            page = int(idx[kvp[b] + p // page_size])
+            if not 0 <= page < num_pages:
+                raise ValueError(f"request {b}: page index {page} outside the cache")
+            kc[page, p % page_size] = kn[ap[b] + i]
+            vc[page, p % page_size] = vn[ap[b] + i]
+    return kc, vc

@@ -173,6 +173,40 @@ def chunked_calls(store: PagedStore, chunk: int) -> list:
     return calls
 
 
+def new_kv_rows(call: Call):
+    """K/V rows [total_q, Hkv, D] of a call's new tokens, in call order: the
+    same seeded rows the store holds at those positions (for append)."""
+    st = call.store
+    ks, vs = [], []
+    for (si, a, b) in call.parts:
+        s = st.seqs[si]
+        base = 4 * int(s.seed)
+        for rows, sub in ((ks, 2), (vs, 3)):
+            full = draw_normal_bf16((s.length, st.num_kv_heads, st.head_dim), base + sub,
+                                    st.device)
+            rows.append(full[s.prefix + a:s.prefix + b])
+    empty = torch.zeros((0, st.num_kv_heads, st.head_dim), dtype=BF16, device=st.device)
+    k = torch.cat(ks, 0) if ks else empty
+    v = torch.cat(vs, 0) if vs else empty
+    return k.contiguous(), v.contiguous()
+
+
+def clear_slots(call: Call, k_cache: torch.Tensor, v_cache: torch.Tensor, value=float("nan")):
+    """Overwrite the cache slots of a call's new tokens with `value`."""
+    P = call.store.page_size
+    for (si, a, b), pages in zip(call.parts, _part_pages(call)):
+        s = call.store.seqs[si]
+        for p in range(s.prefix + a, s.prefix + b):
+            page = int(pages[p // P])
+            k_cache[page, p % P] = value
+            v_cache[page, p % P] = value
+
+
+def _part_pages(call: Call):
+    kvp = call.kv_indptr.tolist()
+    return [call.kv_indices[kvp[i]:kvp[i + 1]] for i in range(call.batch)]
+
+
 def bf16_bits(t: torch.Tensor):
     """Raw bf16 bit patterns of a tensor as a CPU numpy uint16 array."""
     import numpy as np
