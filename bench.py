@@ -348,6 +348,21 @@ def run_sweep(args):
                 bia.bia_set_profile_events(None, None)
         return f
 
+    def append_fn(store, call, k_new, v_new):
+        st = store
+        desc = bia.make_desc(st.num_qo_heads, st.num_kv_heads, st.head_dim, st.page_size)
+        ap, kvp, idx, last = dev_idx(call)
+
+        def f(evs):
+            if evs:
+                evs[0].record(stream)
+            bia.bia_append_paged_kv(desc, k_new, v_new, st.k_cache, st.v_cache, ap, kvp, idx,
+                                    last, call.qo_indptr, call.kv_indptr, call.kv_last_page_len,
+                                    stream=stream)
+            if evs:
+                evs[1].record(stream)
+        return f
+
     def emit(name, kind, work, call_ms, kern_ms, extra=None):
         if kind == "prefill":
             v, u, pk = work / call_ms / 1e9, "TFLOP/s", peaks["bf16_tflops"]
@@ -373,7 +388,12 @@ def run_sweep(args):
     c = wl.whole_prefill(st)
     cm, km = time_calls([prefill_fn(st, c)])
     emit("cfg2 batched prefill (8 req, U[512,8192])", "prefill", prefill_flops(c, D, Hq), cm, km)
-    del st, c
+    k_new, v_new = wl.new_kv_rows(c)
+    cm, km = time_calls([append_fn(st, c, k_new, v_new)])
+    # read the new rows once, write them once
+    emit("paged-KV append of the cfg2 prompts (8 req, U[512,8192], page 1)", "append",
+         4 * k_new.numel() * k_new.element_size(), cm, km)
+    del st, c, k_new, v_new
     st = wl.cfg3_prefix(dev)
     whole = wl.whole_prefill(st)
     cm, km = time_calls([prefill_fn(st, whole)])

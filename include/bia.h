@@ -185,6 +185,37 @@ BIA_API int bia_merge_states(const float *v, const float *s, const int32_t *num_
                      int32_t num_states_max, int32_t num_heads, int32_t head_dim, void *out,
                      float *out_lse, void *stream);
 
+/*
+ * Paged-KV append: writes the key and value rows of a call's new tokens into
+ * their pages, the step that precedes an extend over the same page tables
+ * (the pages' chunked prefill attends each chunk against a cache that already
+ * holds that chunk: "sglang PR #43612", Summary; they never spell the write
+ * out, so it is defined here).  Request b's page table already covers its
+ * n_new(b) = append_indptr[b+1] - append_indptr[b] new tokens as the LAST
+ * n_new(b) of its kv_len keys (the convention bia_prefill_paged uses for q):
+ * new token t of request b is written to position
+ *   kv_len(b) - n_new(b) + (t - append_indptr[b]),
+ * i.e. page kv_indices[kv_indptr[b] + pos / page_size], slot pos % page_size,
+ * all num_kv_heads heads.  Nothing else in the caches is touched.
+ *   k_new, v_new:  [total_new, num_kv_heads, head_dim] bf16, total_new =
+ *                  append_indptr[batch]; 16-byte aligned (as are the caches)
+ *   append_indptr: [batch+1] int32, append_indptr[0] == 0, n_new(b) <= kv_len(b)
+ *   kv_*:          the page table of bia_prefill_paged (num_qo_heads and
+ *                  sm_scale of desc are not used)
+ *   status:        NULL, or a device int32 the call zeroes and then sets bit 0
+ *                  of when a page index is outside [0, num_pages) (that token
+ *                  is skipped); readable with bia_read_status(status, ...)
+ * Two positions that map to the same page slot are the caller's error (which
+ * write lands is then unspecified).
+ */
+BIA_API int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void *v_new,
+                        void *k_cache, void *v_cache, int64_t num_pages,
+                        const int32_t *append_indptr, const int32_t *kv_indptr,
+                        const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                        const int32_t *append_indptr_host, const int32_t *kv_indptr_host,
+                        const int32_t *kv_last_page_len_host, int32_t batch, int32_t *status,
+                        void *stream);
+
 /* Tokens per q tile for GQA group size G = num_qo_heads / num_kv_heads:
  * 128 / G, the chunk grid on which chunked prefill is guaranteed to be
  * bit-identical ("sglang PR #43612", Summary).  0 if G does not divide 128. */

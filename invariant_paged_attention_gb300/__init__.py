@@ -32,7 +32,8 @@ BIA_DECODE_SPLIT = 2048
 EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged",
            "bia_decode_workspace_size", "bia_merge_states", "bia_q_tile_tokens",
            "bia_status_string", "bia_read_status", "bia_set_profile_events",
-           "bia_launch_count", "bia_last_error", "bia_decode_paged_noalloc")
+           "bia_launch_count", "bia_last_error", "bia_decode_paged_noalloc",
+           "bia_append_paged_kv")
 
 
 class BiaError(RuntimeError):
@@ -91,6 +92,9 @@ def load(path: str = LIB_PATH):
     lib.bia_decode_paged_noalloc.argtypes = [dp, vp, vp, vp, i64, vp, vp, vp, vp, vp, i32, i32,
                                              vp, vp, vp]
     lib.bia_decode_paged_noalloc.restype = ctypes.c_int
+    lib.bia_append_paged_kv.argtypes = [dp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32,
+                                        vp, vp]
+    lib.bia_append_paged_kv.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -184,6 +188,23 @@ def bia_decode_paged_noalloc(desc, q, k_cache, v_cache, kv_indptr, kv_indices, k
         len(kvp) - 1, int(split_size), _ptr(out), _ptr(lse), _stream(stream))
     if rc != BIA_OK:
         raise BiaError(rc, "bia_decode_paged_noalloc")
+
+
+def bia_append_paged_kv(desc, k_new, v_new, k_cache, v_cache, append_indptr, kv_indptr,
+                        kv_indices, kv_last_page_len, append_indptr_host, kv_indptr_host,
+                        kv_last_page_len_host, status=None, stream=None):
+    """Write the new tokens' K/V rows [total_new, Hkv, D] into the last
+    n_new positions of each request's pages (include/bia.h states the rule);
+    `status` is an optional 1-element device int32 tensor."""
+    ap, kvp, last = (_host_i32(append_indptr_host), _host_i32(kv_indptr_host),
+                     _host_i32(kv_last_page_len_host))
+    rc = load().bia_append_paged_kv(
+        ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        k_cache.shape[0], _ptr(append_indptr), _ptr(kv_indptr), _ptr(kv_indices),
+        _ptr(kv_last_page_len), _ptr(ap), _ptr(kvp), _ptr(last), len(ap) - 1, _ptr(status),
+        _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_append_paged_kv")
 
 
 def bia_merge_states(v, s, out, out_lse=None, num_states=None, stream=None):

@@ -63,7 +63,7 @@ int check_desc(const bia_attn_desc *d) {
 // planner will produce.  qo == nullptr: decode (one query per request).
 int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
               const int32_t *last, int32_t batch, int32_t causal, int32_t split, int tile_tokens,
-              int tiles_per_unit, HostPlan *hp) {
+              int tiles_per_unit, int ctas, HostPlan *hp) {
   if (batch <= 0 || !kvp || !last) return BIA_ERR_INVALID_ARG;
   if (split <= 0 || split % bia::kKvBlock != 0) return BIA_ERR_UNSUPPORTED;
   if (qo && qo[0] != 0) return BIA_ERR_INVALID_ARG;
@@ -80,9 +80,10 @@ int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
     if (!qo && kv_len == 0) return BIA_ERR_INVALID_ARG;
     int32_t nsp = 1;
     const int64_t tiles = (q_len + tile_tokens - 1) / tile_tokens;
-    p.n_groups += (tiles + tiles_per_unit - 1) / tiles_per_unit;
+    const int64_t gt = bia::group_tiles(tiles_per_unit, ctas);
+    p.n_groups += (tiles + gt - 1) / gt;
     p.n_units += bia::request_units(static_cast<int32_t>(q_len), static_cast<int32_t>(kv_len),
-                                    tile_tokens, tiles_per_unit, causal, split, &nsp);
+                                    tile_tokens, tiles_per_unit, ctas, causal, split, &nsp);
     if (nsp > 1) p.part_rows += q_len * nsp;
     p.total_q += q_len;
   }
@@ -150,10 +151,11 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   const int G = desc->num_qo_heads / desc->num_kv_heads;
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
   const int tiles_per_unit = decode ? 1 : bia::kPrefillTilesPerUnit;
+  const int ctas = decode ? 1 : bia::kPrefillClusterCtas;
   if (decode) causal = 1;
   HostPlan hp;
   rc = host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal, split,
-                 tile_tokens, tiles_per_unit, &hp);
+                 tile_tokens, tiles_per_unit, ctas, &hp);
   if (rc != BIA_OK) return rc;
   const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows,
                                       desc->num_qo_heads, desc->head_dim);
@@ -175,6 +177,7 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   pa.page_size = desc->page_size;
   pa.tile_tokens = tile_tokens;
   pa.tiles_per_unit = tiles_per_unit;
+  pa.ctas = ctas;
   pa.causal = causal;
   pa.split = split;
   pa.n_groups_expected = hp.n_groups;
@@ -247,9 +250,10 @@ size_t workspace_size(bool decode, const bia_attn_desc *desc, const int32_t *qo_
   const int G = desc->num_qo_heads / desc->num_kv_heads;
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
   const int tiles_per_unit = decode ? 1 : bia::kPrefillTilesPerUnit;
+  const int ctas = decode ? 1 : bia::kPrefillClusterCtas;
   HostPlan hp;
   if (host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, decode ? 1 : causal,
-                split, tile_tokens, tiles_per_unit, &hp) != BIA_OK)
+                split, tile_tokens, tiles_per_unit, ctas, &hp) != BIA_OK)
     return 0;
   return bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows, desc->num_qo_heads,
                           desc->head_dim)
@@ -313,6 +317,64 @@ int bia_merge_states(const float *v, const float *s, const int32_t *num_states, 
                                            head_dim, static_cast<uint16_t *>(out), out_lse,
                                            static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return BIA_ERR_CUDA;
+  __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  return BIA_OK;
+}
+
+int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void *v_new,
+                        void *k_cache, void *v_cache, int64_t num_pages,
+                        const int32_t *append_indptr, const int32_t *kv_indptr,
+                        const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                        const int32_t *append_indptr_host, const int32_t *kv_indptr_host,
+                        const int32_t *kv_last_page_len_host, int32_t batch, int32_t *status,
+                        void *stream) {
+  int rc = check_desc(desc);
+  if (rc != BIA_OK) return rc;
+  if (batch <= 0 || !append_indptr_host || !kv_indptr_host || !kv_last_page_len_host)
+    return BIA_ERR_INVALID_ARG;
+  if (append_indptr_host[0] != 0 || kv_indptr_host[0] < 0) return BIA_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t n_new = static_cast<int64_t>(append_indptr_host[b + 1]) - append_indptr_host[b];
+    const int64_t pages = static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b];
+    if (n_new < 0 || pages < 0) return BIA_ERR_INVALID_ARG;
+    const int32_t last = kv_last_page_len_host[b];
+    if (pages > 0 && (last < 1 || last > desc->page_size)) return BIA_ERR_INVALID_ARG;
+    const int64_t kv_len = pages > 0 ? (pages - 1) * desc->page_size + last : 0;
+    if (kv_len > INT32_MAX / 2) return BIA_ERR_UNSUPPORTED;
+    if (n_new > kv_len) return BIA_ERR_INVALID_ARG;
+  }
+  const int64_t total_new = append_indptr_host[batch];
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return BIA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (status) {
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return cuda_fail("status reset", e);
+  }
+  if (total_new == 0) return BIA_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !append_indptr || !kv_indptr || !kv_indices ||
+      !kv_last_page_len || num_pages <= 0)
+    return BIA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_new) & 15u) || (reinterpret_cast<uintptr_t>(v_new) & 15u) ||
+      (reinterpret_cast<uintptr_t>(k_cache) & 15u) || (reinterpret_cast<uintptr_t>(v_cache) & 15u))
+    return BIA_ERR_INVALID_ARG;
+  bia::AppendArgs a{};
+  a.k_new = static_cast<const uint16_t *>(k_new);
+  a.v_new = static_cast<const uint16_t *>(v_new);
+  a.k_cache = static_cast<uint16_t *>(k_cache);
+  a.v_cache = static_cast<uint16_t *>(v_cache);
+  a.append_indptr = append_indptr;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.kv_last_page_len = kv_last_page_len;
+  a.num_pages = num_pages;
+  a.total_new = total_new;
+  a.batch = batch;
+  a.Hkv = desc->num_kv_heads;
+  a.D = desc->head_dim;
+  a.page_size = desc->page_size;
+  a.status = status;
+  cudaError_t e = bia::launch_append(a, st);
+  if (e != cudaSuccess) return cuda_fail("append kernel launch", e);
   __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   return BIA_OK;
 }

@@ -19,6 +19,7 @@ constexpr int32_t kStatusTimeout = 4;      // a bounded device wait gave up
 constexpr int kTileRows = 128; // q tile rows (GQA-packed)
 constexpr int kKvBlock = 128;  // keys per block of the prefill inner loop
 constexpr int kPrefillTilesPerUnit = 2; // q tiles sharing one K/V stream in a prefill CTA
+constexpr int kPrefillClusterCtas = 2;  // prefill CTAs of a cluster sharing each K/V gather
 
 // Per-request record written by the plan kernel.
 struct ReqInfo {
@@ -68,19 +69,25 @@ __host__ __device__ inline int32_t tile_splits(int32_t q_len, int32_t kv_len, in
   return last < 0 ? 1 : last / split + 1;
 }
 
-// Units of one request: its q tiles grouped tiles_per_unit at a time, each
-// group crossed with the split tiles its last (widest) q tile touches.
+// Units of one request: its q tiles grouped ctas * tiles_per_unit at a time,
+// each group crossed with the split tiles its last (widest) q tile touches;
+// a group's units for one split are `ctas` consecutive units (one per CTA of
+// a cluster, tiles_per_unit tiles each; the last ones may hold no tile).
+__host__ __device__ inline int32_t group_tiles(int32_t tiles_per_unit, int32_t ctas) {
+  return tiles_per_unit * ctas;
+}
 __host__ __device__ inline int64_t request_units(int32_t q_len, int32_t kv_len,
                                                  int32_t tile_tokens, int32_t tiles_per_unit,
-                                                 int32_t causal, int32_t split,
+                                                 int32_t ctas, int32_t causal, int32_t split,
                                                  int32_t *max_splits) {
   const int32_t tiles = (q_len + tile_tokens - 1) / tile_tokens;
+  const int32_t gt = group_tiles(tiles_per_unit, ctas);
   int64_t units = 0;
   int32_t nsp = 1;
-  for (int32_t t0 = 0; t0 < tiles; t0 += tiles_per_unit) {
-    const int32_t last = min(t0 + tiles_per_unit, tiles) - 1;
+  for (int32_t t0 = 0; t0 < tiles; t0 += gt) {
+    const int32_t last = min(t0 + gt, tiles) - 1;
     const int32_t n = tile_splits(q_len, kv_len, last, tile_tokens, causal, split);
-    units += n;
+    units += static_cast<int64_t>(n) * ctas;
     if (n > nsp) nsp = n;
   }
   if (max_splits) *max_splits = nsp;
@@ -107,7 +114,7 @@ struct PlanArgs {
   const int32_t *qo_indptr;  // NULL for decode (one token per request)
   const int32_t *kv_indptr;
   const int32_t *kv_last_page_len;
-  int32_t batch, page_size, tile_tokens, tiles_per_unit, causal, split;
+  int32_t batch, page_size, tile_tokens, tiles_per_unit, ctas, causal, split;
   int64_t n_groups_expected, n_units_expected, part_rows_expected;
   int32_t *status;
   ReqInfo *reqs;
@@ -138,7 +145,19 @@ struct AttnArgs {
   int32_t q_rows, kv_rows; // row extents of the maps (a row >= extent reads as zeros)
 };
 
+// Paged-KV append: new token t of request b goes to position
+// kv_len(b) - n_new(b) + (t - append_indptr[b]).
+struct AppendArgs {
+  const uint16_t *k_new, *v_new; // [total_new, Hkv, D]
+  uint16_t *k_cache, *v_cache;
+  const int32_t *append_indptr, *kv_indptr, *kv_indices, *kv_last_page_len;
+  int64_t num_pages, total_new;
+  int32_t batch, Hkv, D, page_size;
+  int32_t *status; // may be NULL
+};
+
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t s);

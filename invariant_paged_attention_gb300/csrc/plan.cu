@@ -8,7 +8,7 @@
 //   B. per group (all threads): its split count
 //   C. block scan of the split counts: each group's first unit
 //   D. per group: its units (the request's last groups first: they carry the
-//      most keys)
+//      most keys); for each split, one unit per CTA of a cluster
 //
 // The host sizes the launch from its mirrors of the same arrays; when the
 // device arrays disagree, every unit is disabled and a status bit is set
@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   __shared__ int64_t s_scan[kPlanThreads];
   __shared__ int s_ok;
   const int tid = threadIdx.x;
+  const int32_t gt = group_tiles(a.tiles_per_unit, a.ctas);
   if (tid == 0) a.status[0] = 0;
 
   // ---- A: per request
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
     const int32_t nsp = tiles > 0 ? tile_splits(q_len, kv_len, tiles - 1, a.tile_tokens,
                                                 a.causal, a.split) : 1;
-    my_groups += (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+    my_groups += (tiles + gt - 1) / gt;
     if (nsp > 1) my_rows += static_cast<int64_t>(q_len) * nsp;
   }
   int64_t total_groups, total_rows;
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     r.pad = 0;
     a.reqs[b] = r;
     a.group_off[b] = static_cast<int32_t>(group);
-    group += (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+    group += (tiles + gt - 1) / gt;
     row += rows;
   }
   __syncthreads();
@@ -120,12 +121,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       const int b = find_group_owner(a.group_off, a.batch, g);
       const ReqInfo r = a.reqs[b];
       const int32_t tiles = (r.q_len + a.tile_tokens - 1) / a.tile_tokens;
-      const int32_t groups = (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+      const int32_t groups = (tiles + gt - 1) / gt;
       const int32_t gi = groups - 1 - (g - a.group_off[b]);
-      const int32_t t0 = gi * a.tiles_per_unit;
-      const int32_t nt = min(a.tiles_per_unit, tiles - t0);
-      a.group_cnt[g] = tile_splits(r.q_len, r.kv_len, t0 + nt - 1, a.tile_tokens, a.causal,
-                                   a.split);
+      const int32_t t0 = gi * gt;
+      const int32_t nt = min(gt, tiles - t0);
+      a.group_cnt[g] = a.ctas * tile_splits(r.q_len, r.kv_len, t0 + nt - 1, a.tile_tokens,
+                                            a.causal, a.split);
     }
   }
   __syncthreads();
@@ -154,14 +155,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int b = find_group_owner(a.group_off, a.batch, g);
     const ReqInfo r = a.reqs[b];
     const int32_t tiles = (r.q_len + a.tile_tokens - 1) / a.tile_tokens;
-    const int32_t groups = (tiles + a.tiles_per_unit - 1) / a.tiles_per_unit;
+    const int32_t groups = (tiles + gt - 1) / gt;
     const int32_t gi = groups - 1 - (g - a.group_off[b]);
-    const int32_t t0 = gi * a.tiles_per_unit;
-    const int32_t nt = min(a.tiles_per_unit, tiles - t0);
+    const int32_t t0 = gi * gt;
+    const int32_t nt = min(gt, tiles - t0);
     const int32_t n = tile_splits(r.q_len, r.kv_len, t0 + nt - 1, a.tile_tokens, a.causal,
                                   a.split);
     int64_t u = a.group_cnt[g];
-    for (int32_t s = 0; s < n; ++s) a.units[u++] = Unit{b, t0, s, nt};
+    for (int32_t s = 0; s < n; ++s)
+      for (int32_t c = 0; c < a.ctas; ++c) {
+        const int32_t tc = t0 + c * a.tiles_per_unit;
+        a.units[u++] = Unit{b, tc, s, max(0, min(a.tiles_per_unit, tiles - tc))};
+      }
   }
 }
 

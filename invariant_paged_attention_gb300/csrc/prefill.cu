@@ -15,11 +15,20 @@
 //   O (+)= P V     tcgen05.mma with A = P read from TMEM, B = V in shared memory
 // Warp roles (10 warps): 0-3 softmax + epilogue of tile A, 4-7 of tile B,
 // 8 issues the MMAs (one thread) and owns TMEM, 9 gathers the q rows and the
-// paged K/V rows with TMA tile::gather4 (each lane fetches four rows per
+// paged K/V rows with TMA tile::gather4 (each gather fetches four rows of one
 // 64-column half; rows past the sequence or on a bad page come from outside
 // the tensor map and read as zeros) into a two-stage ring.  mbarriers order
 // the roles; the MMA order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one
 // tile's softmax overlap the other tile's MMAs.
+//
+// Two CTAs form a cluster: the next two q tiles of the same request, kv head
+// and split.  They read the same K/V blocks, so each CTA gathers half of every
+// block's rows and multicasts them into both CTAs' rings; a stage is refilled
+// once both CTAs' MMAs have released it (multicast commits, barriers counting
+// two arrivals).  This halves the gather requests per SM, which bound the
+// single-CTA version (small 128-byte rows, little of the L2 bandwidth used).
+// Both CTAs walk the union of their tiles' blocks; a CTA waits for and
+// releases the blocks its own tiles do not need without computing on them.
 //
 // Invariance: every reduction boundary is a function of absolute key
 // positions and the split size.  A row's block sequence is the same in any
@@ -36,6 +45,8 @@ namespace bia {
 
 namespace {
 
+constexpr int kCtas = kPrefillClusterCtas;
+constexpr uint16_t kClusterMask = (1u << kCtas) - 1;
 constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp = 9;
 constexpr int kThreads = 320;
@@ -146,25 +157,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   if (blockIdx.x >= a.n_units) return;
   const Unit u = a.units[blockIdx.x];
-  if (u.b < 0) return;
+  if (u.b < 0) return; // plan mismatch: every unit of the launch is disabled
+  const Unit u_peer = a.units[blockIdx.x ^ 1u];
+  const uint32_t rank = cluster_ctarank();
   const ReqInfo r = a.reqs[u.b];
   const int kvh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G, T = a.tile_tokens;
   const int32_t key_begin = u.split * a.split;
 
-  TileInfo ti[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    ti[t].tile = u.tile + t;
-    const bool exists = t < u.ntiles;
-    ti[t].n_splits = exists ? tile_splits(r.q_len, r.kv_len, ti[t].tile, T, a.causal, a.split) : 0;
-    ti[t].has = exists && u.split < ti[t].n_splits;
-    const int32_t last = tile_last_key(r.q_len, r.kv_len, ti[t].tile, T, a.causal);
+  auto tile_info = [&](const Unit &w, int t) {
+    TileInfo x;
+    x.tile = w.tile + t;
+    const bool exists = t < w.ntiles;
+    x.n_splits = exists ? tile_splits(r.q_len, r.kv_len, x.tile, T, a.causal, a.split) : 0;
+    x.has = exists && w.split < x.n_splits;
+    const int32_t last = tile_last_key(r.q_len, r.kv_len, x.tile, T, a.causal);
     const int32_t end = min(key_begin + a.split, last + 1);
-    ti[t].n_blocks = (ti[t].has && end > key_begin) ? (end - key_begin + kKvBlock - 1) / kKvBlock : 0;
-  }
-  const int n_blocks = max(ti[0].n_blocks, ti[1].n_blocks);
+    x.n_blocks = (x.has && end > key_begin) ? (end - key_begin + kKvBlock - 1) / kKvBlock : 0;
+    return x;
+  };
+  TileInfo ti[2];
+  ti[0] = tile_info(u, 0);
+  ti[1] = tile_info(u, 1);
+  const bool any_tile = ti[0].has || ti[1].has;
+  // blocks the cluster moves: the union of both CTAs' tiles
+  const int n_blocks = max(max(ti[0].n_blocks, ti[1].n_blocks),
+                           max(tile_info(u_peer, 0).n_blocks, tile_info(u_peer, 1).n_blocks));
 
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (tid == 0) {
@@ -172,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kVFull + s), 1);
-      mbar_init(bar(L::kKEmpty + s), 1);
-      mbar_init(bar(L::kVEmpty + s), 1);
+      mbar_init(bar(L::kKEmpty + s), kCtas); // one release from each CTA's MMAs
+      mbar_init(bar(L::kVEmpty + s), kCtas);
       mbar_init(bar(L::kSFull + s), 1);
       mbar_init(bar(L::kPFull + s), 4);
       mbar_init(bar(L::kODone + s), 1);
@@ -181,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     fence_mbar_init();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync(); // both CTAs' barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D)
@@ -191,28 +210,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     const int page_mask = (1 << a.page_shift) - 1;
-    if (lane == 0) mbar_expect_tx(bar(L::kQFull), 2u * L::kTile);
-    __syncwarp();
+    if (any_tile) {
+      if (lane == 0) mbar_expect_tx(bar(L::kQFull), 2u * L::kTile);
+      __syncwarp();
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      int32_t rows[4];
+      for (int t = 0; t < 2; ++t) {
+        int32_t rows[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rr = 4 * lane + i;
-        const int32_t tl = ti[t].tile * T + rr / G;
-        const bool ok = ti[t].has && tl < r.q_len;
-        rows[i] = ok ? (r.q_start + tl) * a.Hq + kvh * G + rr % G : a.q_rows;
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * lane + i;
+          const int32_t tl = ti[t].tile * T + rr / G;
+          const bool ok = ti[t].has && tl < r.q_len;
+          rows[i] = ok ? (r.q_start + tl) * a.Hq + kvh * G + rr % G : a.q_rows;
+        }
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+          tma_gather4(sQ(t) + h * kAtom + lane * 512, &a.tm_q, 64 * h, rows[0], rows[1],
+                      rows[2], rows[3], bar(L::kQFull));
       }
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h)
-        tma_gather4(sQ(t) + h * kAtom + lane * 512, &a.tm_q, 64 * h, rows[0], rows[1], rows[2],
-                    rows[3], bar(L::kQFull));
     }
-    // page indices of this lane's four keys of block j (one block ahead)
+    // This CTA gathers rows [64*rank, 64*rank+64) of every block for both
+    // CTAs: lane = 4-row group (lane & 15) x 64-column half (lane >> 4).
+    const int rg = lane & 15, hh = lane >> 4;
+    const bool issues = hh < D / 64;
+    const int32_t row0 = 64 * static_cast<int32_t>(rank) + 4 * rg;
+    const uint32_t dst_off = static_cast<uint32_t>(hh * kAtom + (row0 / 4) * 512);
     auto fetch = [&](int j, int32_t (&pg)[4]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int32_t key = key_begin + j * kKvBlock + 4 * lane + i;
+        const int32_t key = key_begin + j * kKvBlock + row0 + i;
         pg[i] = (j < n_blocks && key < r.kv_len)
                     ? __ldg(a.kv_indices + r.page_base + (key >> a.page_shift)) : -1;
       }
@@ -224,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       int32_t rows[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int32_t key = key_begin + j * kKvBlock + 4 * lane + i;
+        const int32_t key = key_begin + j * kKvBlock + row0 + i;
         rows[i] = a.kv_rows; // outside the map: zeros
         if (key < r.kv_len) {
           if (pg[i] < 0 || pg[i] >= a.num_pages)
@@ -237,31 +263,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       bool ok = j < 2 || mbar_wait(bar(L::kKEmpty + st), ((j >> 1) - 1) & 1, a.status);
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_expect_tx(bar(L::kKFull + st), L::kTile);
+      if (lane == 0) mbar_expect_tx(bar(L::kKFull + st), L::kTile); // both halves land here
       __syncwarp();
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h)
-        tma_gather4(sK(st) + h * kAtom + lane * 512, &a.tm_k, 64 * h, rows[0], rows[1], rows[2],
-                    rows[3], bar(L::kKFull + st));
+      if (issues)
+        tma_gather4_mc(sK(st) + dst_off, &a.tm_k, 64 * hh, rows[0], rows[1], rows[2], rows[3],
+                       bar(L::kKFull + st), kClusterMask);
       ok = j < 2 || mbar_wait(bar(L::kVEmpty + st), ((j >> 1) - 1) & 1, a.status);
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_expect_tx(bar(L::kVFull + st), L::kTile);
       __syncwarp();
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h)
-        tma_gather4(sV(st) + h * kAtom + lane * 512, &a.tm_v, 64 * h, rows[0], rows[1], rows[2],
-                    rows[3], bar(L::kVFull + st));
+      if (issues)
+        tma_gather4_mc(sV(st) + dst_off, &a.tm_v, 64 * hh, rows[0], rows[1], rows[2], rows[3],
+                       bar(L::kVFull + st), kClusterMask);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait(bar(L::kQFull), 0, a.status);
+      bool ok = !any_tile || mbar_wait(bar(L::kQFull), 0, a.status);
+      auto wait_k = [&](int j) {
+        ok = ok && mbar_wait(bar(L::kKFull + (j & 1)), (j >> 1) & 1, a.status);
+        if (ok) tc_fence_after();
+      };
       auto issue_s = [&](int t, int j) {
-        const int st = j & 1;
-        ok = ok && mbar_wait(bar(L::kKFull + st), (j >> 1) & 1, a.status);
         if (!ok) return;
-        tc_fence_after();
+        const int st = j & 1;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * kAtom + (kk & 3) * 32;
@@ -281,21 +307,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         if (j == nb - 1) mma_commit(bar(L::kODone + t));
       };
+      // A stage is released (to both CTAs) only when a later block will
+      // refill it: block j is released iff j + 2 < n_blocks, so every
+      // release is awaited and none reaches a CTA that has left.
       const int nb0 = ti[0].n_blocks, nb1 = ti[1].n_blocks;
+      if (n_blocks > 0) wait_k(0);
       if (nb0 > 0) issue_s(0, 0);
       if (nb1 > 0) issue_s(1, 0);
-      if (ok && n_blocks > 0) mma_commit(bar(L::kKEmpty + 0)); // K_0 read by both S(0)
+      if (ok && 2 < n_blocks) mma_commit_mc(bar(L::kKEmpty + 0), kClusterMask);
       for (int j = 0; j < n_blocks && ok; ++j) {
         const int st = j & 1;
         ok = mbar_wait(bar(L::kVFull + st), (j >> 1) & 1, a.status);
         if (!ok) break;
         if (j < nb0) issue_pv(0, j, nb0);
+        if (j + 1 < n_blocks) wait_k(j + 1);
         if (j + 1 < nb0) issue_s(0, j + 1);
         if (j < nb1) issue_pv(1, j, nb1);
         if (j + 1 < nb1) issue_s(1, j + 1);
         if (!ok) break;
-        mma_commit(bar(L::kVEmpty + st));                                // V_j read
-        if (j + 1 < n_blocks) mma_commit(bar(L::kKEmpty + ((j + 1) & 1))); // K_{j+1} read
+        if (j + 2 < n_blocks) mma_commit_mc(bar(L::kVEmpty + st), kClusterMask);
+        if (j + 3 < n_blocks) mma_commit_mc(bar(L::kKEmpty + ((j + 1) & 1)), kClusterMask);
       }
     }
     __syncwarp();
@@ -425,15 +456,26 @@ cudaError_t launch_prefill_d(const AttnArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(static_cast<unsigned>(a.n_units), static_cast<unsigned>(a.Hkv));
-  prefill_kernel<D><<<grid, kThreads, L::kAlloc, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n_units), static_cast<unsigned>(a.Hkv));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<D>, a);
 }
 
 } // namespace
 
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
+  if (a.n_units % kCtas != 0) return cudaErrorInvalidValue; // the planner pairs every unit
   return a.D == 128 ? launch_prefill_d<128>(a, s) : launch_prefill_d<64>(a, s);
 }
 

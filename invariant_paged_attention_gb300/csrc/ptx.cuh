@@ -163,6 +163,31 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int3
                : "memory");
 }
 
+// The same gather, written at the same shared-memory offset of every CTA of
+// the cluster in cta_mask; each destination CTA's barrier at offset `bar`
+// receives the complete_tx of the bytes written into that CTA.
+__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const void *tmap, int32_t x,
+                                               int32_t y0, int32_t y1, int32_t y2, int32_t y3,
+                                               uint32_t bar, uint16_t cta_mask) {
+  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::"
+               "complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
+               ::"r"(dst), "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar),
+               "h"(cta_mask)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster (warp-uniform call sites only).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global->shared copy; zero-fills when !valid (no global read).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
@@ -227,6 +252,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
+}
+// Arrive once on the barrier at offset `bar` of every CTA in cta_mask when the
+// MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::"
+               "cluster.b64 [%0], %1;" ::"r"(bar), "h"(cta_mask)
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

@@ -19,9 +19,11 @@ def desc_of(store, sm_scale=0.0):
                          store.page_size, sm_scale)
 
 
-def run_prefill(call: wl.Call, causal=True, split=0, sm_scale=0.0):
+def run_prefill(call: wl.Call, causal=True, split=0, sm_scale=0.0, k_cache=None, v_cache=None):
     st = call.store
     dev = st.k_cache.device
+    k_cache = st.k_cache if k_cache is None else k_cache
+    v_cache = st.v_cache if v_cache is None else v_cache
     desc = desc_of(st, sm_scale)
     nbytes = bia.bia_prefill_workspace_size(desc, call.qo_indptr, call.kv_indptr,
                                             call.kv_last_page_len, causal, split)
@@ -30,7 +32,7 @@ def run_prefill(call: wl.Call, causal=True, split=0, sm_scale=0.0):
     out = torch.full_like(call.q, float("nan"))
     lse = torch.full((call.total_q, st.num_qo_heads), float("nan"), dtype=torch.float32,
                      device=dev)
-    bia.bia_prefill_paged(desc, call.q, st.k_cache, st.v_cache, call.qo_indptr.to(dev),
+    bia.bia_prefill_paged(desc, call.q, k_cache, v_cache, call.qo_indptr.to(dev),
                           call.kv_indptr.to(dev), call.kv_indices.to(dev),
                           call.kv_last_page_len.to(dev), call.qo_indptr, call.kv_indptr,
                           call.kv_last_page_len, ws, out, lse, causal=causal, split_size=split)

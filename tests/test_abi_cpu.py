@@ -139,6 +139,29 @@ def test_decode_and_merge_reject_bad_arguments_on_the_host(bia):
     assert lib.bia_merge_states(None, None, None, 0, 2, 8, 128, None, None, None) == bia.BIA_OK
 
 
+def test_append_rejects_bad_arguments_on_the_host(bia):
+    lib = bia.load()
+    p = ctypes.c_void_p
+
+    def call(desc, ap, kvp, last, k_new=FAKE, status=None):
+        ap, kvp, last = (torch.tensor(x, dtype=torch.int32) for x in (ap, kvp, last))
+        return lib.bia_append_paged_kv(ctypes.byref(desc), p(k_new), p(FAKE), p(FAKE), p(FAKE),
+                                       1 << 20, p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                                       p(ap.data_ptr()), p(kvp.data_ptr()), p(last.data_ptr()),
+                                       len(ap) - 1, None if status is None else p(status), None)
+    d = bia.make_desc(32, 8, 128, 16)
+    inv = bia.BIA_ERR_INVALID_ARG
+    assert call(d, [0, 17], [0, 1], [16]) == inv  # 17 new tokens, 16 keys
+    assert call(d, [1, 2], [0, 1], [16]) == inv  # append_indptr[0] != 0
+    assert call(d, [0, 2, 1], [0, 1, 2], [16, 16]) == inv  # decreasing append_indptr
+    assert call(d, [0, 1], [0, 1], [0]) == inv  # last page length 0
+    assert call(d, [0, 1], [0, 1], [1], k_new=FAKE + 8) == inv  # unaligned rows
+    assert call(d, [0, 1], [0, 1], [1], status=FAKE + 2) == inv  # unaligned status word
+    assert call(bia.make_desc(32, 8, 256, 16), [0, 1], [0, 1], [1]) == bia.BIA_ERR_UNSUPPORTED
+    # nothing to write and no status word: returns before touching the device
+    assert call(d, [0, 0, 0], [0, 1, 3], [5, 2]) == bia.BIA_OK
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     import invariant_paged_attention_gb300 as m
     saved = m._lib
