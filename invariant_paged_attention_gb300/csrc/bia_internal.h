@@ -19,7 +19,7 @@ constexpr int32_t kStatusTimeout = 4;      // a bounded device wait gave up
 constexpr int kTileRows = 128; // q tile rows (GQA-packed)
 constexpr int kKvBlock = 128;  // keys per block of the prefill inner loop
 constexpr int kPrefillTilesPerUnit = 2; // q tiles sharing one K/V stream in a prefill CTA
-constexpr int kPrefillClusterCtas = 2;  // prefill CTAs of a cluster sharing each K/V gather
+constexpr int kPrefillClusterCtas = 4;  // prefill CTAs of a cluster sharing each K/V gather
 
 // Per-request record written by the plan kernel.
 struct ReqInfo {

@@ -21,14 +21,15 @@
 // the roles; the MMA order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one
 // tile's softmax overlap the other tile's MMAs.
 //
-// Two CTAs form a cluster: the next two q tiles of the same request, kv head
-// and split.  They read the same K/V blocks, so each CTA gathers half of every
-// block's rows and multicasts them into both CTAs' rings; a stage is refilled
-// once both CTAs' MMAs have released it (multicast commits, barriers counting
-// two arrivals).  This halves the gather requests per SM, which bound the
-// single-CTA version (small 128-byte rows, little of the L2 bandwidth used).
-// Both CTAs walk the union of their tiles' blocks; a CTA waits for and
-// releases the blocks its own tiles do not need without computing on them.
+// kPrefillClusterCtas CTAs form a cluster: consecutive q-tile pairs of the
+// same request, kv head and split.  They read the same K/V blocks, so each CTA
+// gathers its share of every block's rows and multicasts them into all the
+// cluster's rings; a stage is refilled once every CTA's MMAs have released it
+// (multicast commits, barriers counting one arrival per CTA).  This divides
+// the gather requests per SM, which bound the single-CTA version (small
+// 128-byte rows, little of the L2 bandwidth used).  All CTAs walk the union
+// of their tiles' blocks; a CTA waits for and releases the blocks its own
+// tiles do not need without computing on them.
 //
 // Invariance: every reduction boundary is a function of absolute key
 // positions and the split size.  A row's block sequence is the same in any
@@ -158,7 +159,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (blockIdx.x >= a.n_units) return;
   const Unit u = a.units[blockIdx.x];
   if (u.b < 0) return; // plan mismatch: every unit of the launch is disabled
-  const Unit u_peer = a.units[blockIdx.x ^ 1u];
   const uint32_t rank = cluster_ctarank();
   const ReqInfo r = a.reqs[u.b];
   const int kvh = blockIdx.y;
@@ -181,9 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   ti[0] = tile_info(u, 0);
   ti[1] = tile_info(u, 1);
   const bool any_tile = ti[0].has || ti[1].has;
-  // blocks the cluster moves: the union of both CTAs' tiles
-  const int n_blocks = max(max(ti[0].n_blocks, ti[1].n_blocks),
-                           max(tile_info(u_peer, 0).n_blocks, tile_info(u_peer, 1).n_blocks));
+  // blocks the cluster moves: the union of all its CTAs' tiles
+  int n_blocks = 0;
+  const unsigned first = blockIdx.x - blockIdx.x % kCtas;
+#pragma unroll
+  for (int c = 0; c < kCtas; ++c) {
+    const Unit w = a.units[first + c];
+    n_blocks = max(n_blocks, max(tile_info(w, 0).n_blocks, tile_info(w, 1).n_blocks));
+  }
 
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (tid == 0) {
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     fence_mbar_init();
   }
   tc_fence_before();
-  cluster_sync(); // both CTAs' barriers exist before any multicast reaches them
+  cluster_sync(); // every CTA's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D)
@@ -229,11 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                       rows[2], rows[3], bar(L::kQFull));
       }
     }
-    // This CTA gathers rows [64*rank, 64*rank+64) of every block for both
-    // CTAs: lane = 4-row group (lane & 15) x 64-column half (lane >> 4).
-    const int rg = lane & 15, hh = lane >> 4;
+    // This CTA gathers its 1/kCtas share of every block's rows for all CTAs
+    // of the cluster: lane = 4-row group x 64-column half.
+    constexpr int kGroups = kKvBlock / kCtas / 4; // 4-row groups per CTA
+    const int rg = lane % kGroups, hh = lane / kGroups;
     const bool issues = hh < D / 64;
-    const int32_t row0 = 64 * static_cast<int32_t>(rank) + 4 * rg;
+    const int32_t row0 = (kKvBlock / kCtas) * static_cast<int32_t>(rank) + 4 * rg;
     const uint32_t dst_off = static_cast<uint32_t>(hh * kAtom + (row0 / 4) * 512);
     auto fetch = [&](int j, int32_t (&pg)[4]) {
 #pragma unroll
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       bool ok = j < 2 || mbar_wait(bar(L::kKEmpty + st), ((j >> 1) - 1) & 1, a.status);
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_expect_tx(bar(L::kKFull + st), L::kTile); // both halves land here
+      if (lane == 0) mbar_expect_tx(bar(L::kKFull + st), L::kTile); // every share lands here
       __syncwarp();
       if (issues)
         tma_gather4_mc(sK(st) + dst_off, &a.tm_k, 64 * hh, rows[0], rows[1], rows[2], rows[3],
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         if (j == nb - 1) mma_commit(bar(L::kODone + t));
       };
-      // A stage is released (to both CTAs) only when a later block will
+      // A stage is released (to every CTA) only when a later block will
       // refill it: block j is released iff j + 2 < n_blocks, so every
       // release is awaited and none reaches a CTA that has left.
       const int nb0 = ti[0].n_blocks, nb1 = ti[1].n_blocks;
