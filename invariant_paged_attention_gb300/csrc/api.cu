@@ -125,6 +125,26 @@ int encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int head_d
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
+// The q tiles of a prefill call as a 3-D map [total_q][Hq][head_dim]; a box
+// of 64 columns x G heads x T tokens is one 64-column half of a 128-row q
+// tile (rows = token-major (token, head) pairs, 128-byte swizzle); tokens past
+// the end read as zeros.
+int encode_q_map(CUtensorMap *map, const void *base, int64_t total_q, int Hq, int head_dim, int G,
+                 int T) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return -1;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(Hq),
+                              static_cast<cuuint64_t>(total_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(Hq) * head_dim * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(T)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return static_cast<int>(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
 float effective_scale(const bia_attn_desc *d) {
   const float s = d->sm_scale > 0.f ? d->sm_scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
   return s * 1.4426950408889634f;
@@ -221,7 +241,8 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   if (!decode) {
     a.q_rows = static_cast<int32_t>(q_rows);
     a.kv_rows = static_cast<int32_t>(kv_rows);
-    int ce = encode_rows_map(&a.tm_q, q, q_rows, desc->head_dim);
+    int ce = encode_q_map(&a.tm_q, q, hp.total_q, desc->num_qo_heads, desc->head_dim, G,
+                          tile_tokens);
     if (ce == 0) ce = encode_rows_map(&a.tm_k, k_cache, kv_rows, desc->head_dim);
     if (ce == 0) ce = encode_rows_map(&a.tm_v, v_cache, kv_rows, desc->head_dim);
     if (ce != 0) return fail(BIA_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable", ce);

@@ -139,8 +139,9 @@ struct AttnArgs {
   uint16_t *out;
   float *lse;
   int32_t *status;
-  // TMA descriptors (prefill): q rows [total_q*Hq, D] and key / value rows
-  // [num_pages*page_size*Hkv, D], 64-column boxes, one row high, SW128
+  // TMA descriptors (prefill): q [total_q][Hq][D] in boxes of 64 columns x G
+  // heads x tile_tokens tokens, and key / value rows [num_pages*page_size*Hkv,
+  // D] in 64-column boxes one row high; all SW128
   CUtensorMap tm_q, tm_k, tm_v;
   int32_t q_rows, kv_rows; // row extents of the maps (a row >= extent reads as zeros)
 };

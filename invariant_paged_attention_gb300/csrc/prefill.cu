@@ -14,10 +14,11 @@
 //                  as bf16 back into the S columns of TMEM (tcgen05.st)
 //   O (+)= P V     tcgen05.mma with A = P read from TMEM, B = V in shared memory
 // Warp roles (10 warps): 0-3 softmax + epilogue of tile A, 4-7 of tile B,
-// 8 issues the MMAs (one thread) and owns TMEM, 9 gathers the q rows and the
-// paged K/V rows with TMA tile::gather4 (each gather fetches four rows of one
-// 64-column half; rows past the sequence or on a bad page come from outside
-// the tensor map and read as zeros) into a two-stage ring.  mbarriers order
+// 8 issues the MMAs (one thread) and owns TMEM, 9 loads the two q tiles (3-D
+// TMA boxes of G heads x 128/G tokens) and gathers the paged K/V rows with TMA
+// tile::gather4 (each gather fetches four rows of one 64-column half; rows
+// past the sequence or on a bad page come from outside the tensor map and
+// read as zeros) into a two-stage ring.  mbarriers order
 // the roles; the MMA order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one
 // tile's softmax overlap the other tile's MMAs.
 //
@@ -204,6 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     fence_mbar_init();
   }
+  __syncthreads();
+  if (warp == kProducerWarp && lane == 0 && any_tile) {
+    // the q tiles (a local load) go out before the cluster handshake
+    mbar_expect_tx(bar(L::kQFull), static_cast<uint32_t>(ti[0].has + ti[1].has) * L::kTile);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      if (ti[t].has)
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sQ(t) + h * kAtom, &a.tm_q, 64 * h, kvh * G, r.q_start + ti[t].tile * T,
+                      bar(L::kQFull));
+  }
   tc_fence_before();
   cluster_sync(); // every CTA's barriers exist before any multicast reaches them
   tc_fence_after();
@@ -215,25 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     const int page_mask = (1 << a.page_shift) - 1;
-    if (any_tile) {
-      if (lane == 0) mbar_expect_tx(bar(L::kQFull), 2u * L::kTile);
-      __syncwarp();
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        int32_t rows[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = 4 * lane + i;
-          const int32_t tl = ti[t].tile * T + rr / G;
-          const bool ok = ti[t].has && tl < r.q_len;
-          rows[i] = ok ? (r.q_start + tl) * a.Hq + kvh * G + rr % G : a.q_rows;
-        }
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h)
-          tma_gather4(sQ(t) + h * kAtom + lane * 512, &a.tm_q, 64 * h, rows[0], rows[1],
-                      rows[2], rows[3], bar(L::kQFull));
-      }
-    }
     // This CTA gathers its 1/kCtas share of every block's rows for all CTAs
     // of the cluster: lane = 4-row group x 64-column half.
     constexpr int kGroups = kKvBlock / kCtas / 4; // 4-row groups per CTA
@@ -343,7 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const TileInfo me = t ? ti[1] : ti[0];
     const int32_t t_row = me.tile * T + row / G;
-    const int h_row = kvh * G + row % G;
     const bool row_valid = me.has && t_row < r.q_len;
     const int32_t p_row = a.causal ? r.kv_len - r.q_len + t_row : r.kv_len - 1;
     const int32_t vis_last = min(p_row, r.kv_len - 1);
@@ -390,55 +383,98 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kPFull + t));
     }
-    // epilogue
+    // epilogue: o_s = O / l row by row into the tile's q buffer (free once
+    // its last MMA is done; rows of D*2 bytes), then copied out by whole rows
+    // so that every global store is coalesced.  bf16 rows for a tile with one
+    // split (one pass), else fp32 partial rows (two passes of D/2 columns).
     if (me.has) {
-      const bool have_o = !failed && me.n_blocks > 0 &&
-                          mbar_wait(bar(L::kODone + t), 0, a.status);
+      // warp-uniform (tcgen05.ld is warp-collective): a warp with a failed
+      // wait writes zeros
+      const bool have_o = __all_sync(0xffffffffu, !failed && me.n_blocks > 0 &&
+                                                      mbar_wait(bar(L::kODone + t), 0, a.status));
       tc_fence_after();
       const bool nonzero = have_o && l > 0.f;
       const float lse = nonzero ? __fmul_rn(__fadd_rn(m, lg2(l)), kLn2) : -INFINITY;
       const float inv_l = nonzero ? __frcp_rn(l) : 0.f; // o_s = O * (1/l)
-      const bool final_row = me.n_splits == 1;
-      const int64_t out_row = static_cast<int64_t>(r.q_start + t_row) * a.Hq + h_row;
-      const int64_t part_row =
-          (r.rowbase + static_cast<int64_t>(t_row) * r.nsp + u.split) * a.Hq + h_row;
+      const bool final_row = me.n_splits == 1;           // uniform over the tile
+      const int gs = __ffs(G) - 1; // G is a power of two
+      auto out_row_of = [&](int rr) {
+        return static_cast<int64_t>(r.q_start + me.tile * T + (rr >> gs)) * a.Hq + kvh * G +
+               (rr & (G - 1));
+      };
+      auto part_row_of = [&](int rr) {
+        return (r.rowbase + static_cast<int64_t>(me.tile * T + (rr >> gs)) * r.nsp + u.split) *
+                   a.Hq +
+               kvh * G + (rr & (G - 1));
+      };
+      uint8_t *stage = smem + L::kQ0 + t * L::kTile; // 128 rows x D*2 bytes
+      constexpr int row_bytes = D * 2;
+      constexpr int chunks = row_bytes / 16; // 16-byte chunks per staged row
+      const int pass_cols = final_row ? D : D / 2;
+      const int n_pass = D / pass_cols;
+      for (int ps = 0; ps < n_pass; ++ps) {
+        // this thread's row: chunk c at position c ^ (row % chunks); O read
+        // 32 columns at a time with the next load in flight
+        uint4 *my = reinterpret_cast<uint4 *>(stage + row * row_bytes);
+        const int nchunk = pass_cols / 32;
+        const uint32_t obase = tO(t) + lane_base + ps * pass_cols;
+        uint32_t v[2][32];
+        if (have_o) tmem_ld32(obase, v[0]);
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        float o[16];
-        if (have_o) {
-          uint32_t v[16];
-          tmem_ld16(tO(t) + lane_base + c * 16, v);
-          tmem_wait_ld();
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+          if (c32 >= nchunk) break;
+          float o[32];
+          if (have_o) {
+            tmem_wait_ld();
+            if (c32 + 1 < nchunk) tmem_ld32(obase + (c32 + 1) * 32, v[(c32 + 1) & 1]);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(__uint_as_float(v[i]), inv_l);
-        } else {
+            for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(__uint_as_float(v[c32 & 1][i]), inv_l);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = 0.f;
-        }
-        if (!row_valid) continue;
-        if (final_row) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.out + out_row * D + c * 16);
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint4 w;
-            w.x = pack_bf16(o[q * 8 + 0], o[q * 8 + 1]);
-            w.y = pack_bf16(o[q * 8 + 2], o[q * 8 + 3]);
-            w.z = pack_bf16(o[q * 8 + 4], o[q * 8 + 5]);
-            w.w = pack_bf16(o[q * 8 + 6], o[q * 8 + 7]);
-            dst[q] = w;
+            for (int i = 0; i < 32; ++i) o[i] = 0.f;
           }
-        } else {
-          float4 *dst = reinterpret_cast<float4 *>(a.part_o + part_row * D + c * 16);
+          if (final_row) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
+            for (int q = 0; q < 4; ++q) {
+              uint4 w;
+              w.x = pack_bf16(o[q * 8 + 0], o[q * 8 + 1]);
+              w.y = pack_bf16(o[q * 8 + 2], o[q * 8 + 3]);
+              w.z = pack_bf16(o[q * 8 + 4], o[q * 8 + 5]);
+              w.w = pack_bf16(o[q * 8 + 6], o[q * 8 + 7]);
+              my[(c32 * 4 + q) ^ (row % chunks)] = w;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              my[(c32 * 8 + q) ^ (row % chunks)] =
+                  make_uint4(__float_as_uint(o[q * 4]), __float_as_uint(o[q * 4 + 1]),
+                             __float_as_uint(o[q * 4 + 2]), __float_as_uint(o[q * 4 + 3]));
+          }
         }
+        bar_sync_named(1 + t, 128);
+        // copy out: each warp takes 32 rows, chunks lanes per row
+        const int tl = (warp & 3) * 32 + lane; // 0..127 within the tile's threads
+        constexpr int rows_per_step = 128 / chunks; // rows the 128 threads cover per step
+#pragma unroll 4
+        for (int r0 = 0; r0 < kTileRows; r0 += rows_per_step) {
+          const int rr = r0 + tl / chunks, c = tl % chunks;
+          const int32_t t_rr = me.tile * T + (rr >> gs);
+          if (t_rr < r.q_len) {
+            const uint4 w =
+                reinterpret_cast<const uint4 *>(stage + rr * row_bytes)[c ^ (rr % chunks)];
+            if (final_row)
+              reinterpret_cast<uint4 *>(a.out + out_row_of(rr) * D)[c] = w;
+            else
+              reinterpret_cast<uint4 *>(a.part_o + part_row_of(rr) * D + ps * pass_cols)[c] = w;
+          }
+        }
+        bar_sync_named(1 + t, 128); // the stage is rewritten by the next pass
       }
       if (row_valid) {
         if (final_row) {
-          if (a.lse) a.lse[out_row] = lse;
+          if (a.lse) a.lse[out_row_of(row)] = lse;
         } else {
-          a.part_lse[part_row] = lse;
+          a.part_lse[part_row_of(row)] = lse;
         }
       }
     }

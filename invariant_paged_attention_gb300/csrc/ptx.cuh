@@ -163,6 +163,16 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int3
                : "memory");
 }
 
+// A 3-D tiled TMA load (coordinates innermost first) into this CTA's shared
+// memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                            int32_t z, uint32_t bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+               "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+               : "memory");
+}
+
 // The same gather, written at the same shared-memory offset of every CTA of
 // the cluster in cta_mask; each destination CTA's barrier at offset `bar`
 // receives the complete_tx of the bytes written into that CTA.
@@ -174,6 +184,11 @@ __device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const void *tmap, i
                ::"r"(dst), "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar),
                "h"(cta_mask)
                : "memory");
+}
+
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- clusters
