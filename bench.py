@@ -52,7 +52,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true",
                    help="skip the oracle CPU baseline (quick runs)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
-    p.add_argument("--cpu-seconds", type=float, default=12.0,
+    p.add_argument("--cpu-seconds", type=float, default=20.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--only", choices=["both", "prefill", "decode"], default="both",
                    help="run one of the two calls (profiling captures of a small case)")
