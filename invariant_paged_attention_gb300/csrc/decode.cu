@@ -1,4 +1,5 @@
-// Split-KV paged decode: one CTA per (request, split-KV tile, kv head).
+// Split-KV paged decode: one CTA per (request, split-KV tile, kv head), the kv
+// heads of a (request, split) adjacent in the grid.
 //
 // The split's keys are cut into chunks of 8 consecutive keys; warp w of the
 // CTA owns chunks w, w+8, w+16, ...  Each warp streams its chunks' key and
@@ -115,11 +116,13 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
   const uint32_t sbase = smem_u32(smem);
 
-  if (blockIdx.x >= a.n_units) return;
-  const Unit u = a.units[blockIdx.x];
+  // block = unit * Hkv + kv head: the kv heads of a unit run side by side
+  const int64_t unit = blockIdx.x / a.Hkv;
+  const int kvh = static_cast<int>(blockIdx.x - unit * a.Hkv);
+  if (unit >= a.n_units) return;
+  const Unit u = a.units[unit];
   if (u.b < 0) return;
   const ReqInfo r = a.reqs[u.b];
-  const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPK, sub = lane % LPK;
   const int32_t key_begin = u.split * a.split;
@@ -376,8 +379,9 @@ cudaError_t launch_decode_dg(const AttnArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(static_cast<unsigned>(a.n_units), static_cast<unsigned>(a.Hkv));
-  decode_kernel<D, G><<<grid, kThreadsDec, L::kAlloc, s>>>(a);
+  const int64_t blocks = a.n_units * a.Hkv;
+  if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
+  decode_kernel<D, G><<<static_cast<unsigned>(blocks), kThreadsDec, L::kAlloc, s>>>(a);
   return cudaGetLastError();
 }
 
