@@ -52,6 +52,10 @@ def _load():
                                                   vp, vp, vp, i32, i64, i64, vp, i64, vp, vp,
                                                   i32]
             lib.oracle_attention_rows.restype = i32
+            lib.oracle_attention_rows_masked.argtypes = [i32, i32, i32, i32, f64, i32, vp, vp,
+                                                         vp, vp, vp, vp, vp, i32, i64, i64, vp,
+                                                         vp, vp, i64, vp, vp, i32]
+            lib.oracle_attention_rows_masked.restype = i32
             lib.oracle_row_probs.argtypes = [i32, i32, i32, i32, f64, i32, vp, vp, vp, vp, vp,
                                              vp, vp, i32, i64, i32, vp, i64]
             lib.oracle_row_probs.restype = i32
@@ -85,15 +89,19 @@ def default_threads() -> int:
 
 def attention(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, *,
               num_qo_heads, num_kv_heads, head_dim, page_size, causal=True, sm_scale=None,
-              rows=None, key_window=None, threads=None):
+              rows=None, key_window=None, threads=None, mask=None, mask_indptr=None):
     """Paged GQA attention in fp64.
 
     q: [total_q, Hq, D] uint16 (bf16 bits); k_cache / v_cache:
     [num_pages, page_size, Hkv, D] uint16.  ``rows`` is an optional int64
     array of (global q token, q head) pairs; without it every row is computed.
     ``key_window=(lo, hi)`` restricts visible keys to [lo, hi) (a split-KV
-    partial).  Returns (out [n, D] float64, lse [n] float64); with rows=None
-    the shapes are [total_q, Hq, D] and [total_q, Hq].
+    partial).  ``mask`` (uint8, little-endian bit order) with ``mask_indptr``
+    (int64 bit offsets, [batch+1]) is a custom mask: bit
+    mask_indptr[b] + t*kv_len + j lets in-call token t of request b see key j
+    (together with the causal rule when causal).  Returns (out [n, D]
+    float64, lse [n] float64); with rows=None the shapes are
+    [total_q, Hq, D] and [total_q, Hq].
     """
     lib = _load()
     q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
@@ -111,11 +119,17 @@ def attention(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_pag
         n = rows_arr.shape[0]
     out = np.zeros((max(n, 1), head_dim), np.float64)
     lse = np.zeros(max(n, 1), np.float64)
-    rc = lib.oracle_attention_rows(num_qo_heads, num_kv_heads, head_dim, page_size, scale,
-                                   int(bool(causal)), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                                   _ptr(qo), _ptr(kvp), _ptr(kvi), _ptr(last), batch, int(lo),
-                                   int(hi), None if rows_arr is None else _ptr(rows_arr), n,
-                                   _ptr(out), _ptr(lse), threads or default_threads())
+    if mask is not None:
+        mask_arr = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
+        if mask_arr.size == 0:
+            mask_arr = np.zeros(1, np.uint8)
+        mip = np.ascontiguousarray(np.asarray(mask_indptr, dtype=np.int64))
+    rc = lib.oracle_attention_rows_masked(
+        num_qo_heads, num_kv_heads, head_dim, page_size, scale, int(bool(causal)), _ptr(q),
+        _ptr(k_cache), _ptr(v_cache), _ptr(qo), _ptr(kvp), _ptr(kvi), _ptr(last), batch, int(lo),
+        int(hi), None if mask is None else _ptr(mask_arr), None if mask is None else _ptr(mip),
+        None if rows_arr is None else _ptr(rows_arr), n, _ptr(out), _ptr(lse),
+        threads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_attention_rows failed with {rc}")
     out, lse = out[:n], lse[:n]

@@ -25,7 +25,11 @@
  *     sees keys 0..p, a non-causal row sees all kv_len keys;
  *   - s_j = sm_scale * <q, k_j>, out = sum_j e^{s_j-m} v_j / sum_j e^{s_j-m},
  *     lse = m + ln sum_j e^{s_j-m} (natural log), m = max_j s_j;
- *   - a row that sees no key has out = 0 and lse = -inf.
+ *   - a row that sees no key has out = 0 and lse = -inf;
+ *   - an optional custom mask (the pages name none; it follows the bit-packed
+ *     per-request [q_len, kv_len] mask of paged prefill wrappers) removes
+ *     further keys: key j is visible to in-call token t of request b only if
+ *     bit mask_indptr[b] + t*kv_len + j of the little-endian bit string is 1.
  *
  * An optional key window [key_lo, key_hi) restricts the visible keys further;
  * with the window set to one split-KV tile it yields that split's partial
@@ -63,7 +67,21 @@ typedef struct {
     const int64_t *rows; /* pairs (global q token, q head); NULL = every row */
     int64_t n_rows;
     double *out, *lse;
+    /* optional custom mask: bit (mask_indptr[b] + t*kv_len + j) of the
+     * little-endian bit string `mask` says whether in-call token t of
+     * request b may see key j (on top of the causal rule when causal) */
+    const uint8_t *mask;
+    const int64_t *mask_indptr;
 } oracle_problem;
+
+/* Whether row (request b, in-call token tl) may see key j by the custom mask. */
+static int mask_allows(const oracle_problem *pb, int b, int64_t tl, int64_t kv_len, int64_t j)
+{
+    if (!pb->mask)
+        return 1;
+    int64_t bit = pb->mask_indptr[b] + tl * kv_len + j;
+    return (pb->mask[bit >> 3] >> (bit & 7)) & 1;
+}
 
 static int64_t request_kv_len(const oracle_problem *pb, int b)
 {
@@ -126,8 +144,15 @@ static void attend_row(const oracle_problem *pb, int64_t t, int h, double *score
         return;
     }
 
+    const int64_t tl = t - pb->qo_indptr[b];
     double m = -INFINITY;
+    int any = 0;
     for (int64_t j = first; j <= last; j++) {
+        if (!mask_allows(pb, b, tl, kv_len, j)) {
+            scores[j - first] = -INFINITY;
+            continue;
+        }
+        any = 1;
         const uint16_t *krow = paged_row(pb, pb->k_cache, b, j, g);
         double dot = 0.0;
         for (int d = 0; d < D; d++)
@@ -137,13 +162,23 @@ static void attend_row(const oracle_problem *pb, int64_t t, int h, double *score
         if (s > m)
             m = s;
     }
+    if (!any) {
+        *lse = -INFINITY;
+        return;
+    }
     double denom = 0.0;
     for (int64_t j = first; j <= last; j++) {
+        if (scores[j - first] == -INFINITY) {
+            scores[j - first] = 0.0;
+            continue;
+        }
         double w = exp(scores[j - first] - m);
         scores[j - first] = w;
         denom += w;
     }
     for (int64_t j = first; j <= last; j++) {
+        if (scores[j - first] == 0.0)
+            continue;
         const uint16_t *vrow = paged_row(pb, pb->v_cache, b, j, g);
         double w = scores[j - first] / denom;
         for (int d = 0; d < D; d++)
@@ -190,21 +225,25 @@ static void *run_slice(void *arg)
  * over (token, head)).  key_lo/key_hi bound the visible keys (pass 0 and
  * INT64_MAX for the plain attention).  Returns 0 or a negative code.
  */
-int oracle_attention_rows(int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                          int32_t page_size, double sm_scale, int32_t causal, const uint16_t *q,
-                          const uint16_t *k_cache, const uint16_t *v_cache,
-                          const int32_t *qo_indptr, const int32_t *kv_indptr,
-                          const int32_t *kv_indices, const int32_t *kv_last_page_len,
-                          int32_t batch, int64_t key_lo, int64_t key_hi, const int64_t *rows,
-                          int64_t n_rows, double *out, double *lse, int32_t n_threads)
+int oracle_attention_rows_masked(int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t page_size, double sm_scale, int32_t causal,
+                                 const uint16_t *q, const uint16_t *k_cache,
+                                 const uint16_t *v_cache, const int32_t *qo_indptr,
+                                 const int32_t *kv_indptr, const int32_t *kv_indices,
+                                 const int32_t *kv_last_page_len, int32_t batch, int64_t key_lo,
+                                 int64_t key_hi, const uint8_t *mask, const int64_t *mask_indptr,
+                                 const int64_t *rows, int64_t n_rows, double *out, double *lse,
+                                 int32_t n_threads)
 {
     if (num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0 ||
         head_dim <= 0 || page_size <= 0 || batch <= 0 || !q || !k_cache || !v_cache ||
-        !qo_indptr || !kv_indptr || !kv_indices || !kv_last_page_len || !out || !lse)
+        !qo_indptr || !kv_indptr || !kv_indices || !kv_last_page_len || !out || !lse ||
+        (mask && !mask_indptr))
         return ORACLE_BAD_ARG;
     oracle_problem pb = {num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, causal,
                          q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices,
-                         kv_last_page_len, batch, key_lo, key_hi, rows, n_rows, out, lse};
+                         kv_last_page_len, batch, key_lo, key_hi, rows, n_rows, out, lse,
+                         mask, mask_indptr};
     int64_t total = rows ? n_rows : (int64_t)qo_indptr[batch] * num_qo_heads;
     int64_t max_kv = 0;
     for (int b = 0; b < batch; b++) {
@@ -240,6 +279,21 @@ int oracle_attention_rows(int32_t num_qo_heads, int32_t num_kv_heads, int32_t he
             status = sl[i].status;
     }
     return status;
+}
+
+/* oracle_attention_rows_masked without a custom mask. */
+int oracle_attention_rows(int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t page_size, double sm_scale, int32_t causal, const uint16_t *q,
+                          const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *qo_indptr, const int32_t *kv_indptr,
+                          const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                          int32_t batch, int64_t key_lo, int64_t key_hi, const int64_t *rows,
+                          int64_t n_rows, double *out, double *lse, int32_t n_threads)
+{
+    return oracle_attention_rows_masked(num_qo_heads, num_kv_heads, head_dim, page_size,
+                                        sm_scale, causal, q, k_cache, v_cache, qo_indptr,
+                                        kv_indptr, kv_indices, kv_last_page_len, batch, key_lo,
+                                        key_hi, NULL, NULL, rows, n_rows, out, lse, n_threads);
 }
 
 /*

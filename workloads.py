@@ -207,6 +207,30 @@ def _part_pages(call: Call):
     return [call.kv_indices[kvp[i]:kvp[i + 1]] for i in range(call.batch)]
 
 
+def custom_mask(call: Call, seed: int, density: float = 0.7, causal_part: bool = False):
+    """A seeded custom mask for a call: per request a [q_len, kv_len] boolean
+    matrix (True = the token may see the key), i.i.d. Bernoulli(density), and
+    optionally AND-ed with the bottom-right causal pattern.  Returns
+    (bits uint8 [little-endian bit order], indptr int64 [batch+1] bit offsets,
+    list of the dense matrices)."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    dense, flat, offs = [], [], [0]
+    for ql, kl in zip(call.q_lens, call.kv_lens):
+        m = rng.random((ql, kl)) < density
+        if causal_part:
+            pos = kl - ql + np.arange(ql)
+            m &= np.arange(kl)[None, :] <= pos[:, None]
+        dense.append(m)
+        flat.append(m.reshape(-1))
+        offs.append(offs[-1] + ql * kl)
+    bits = np.concatenate(flat) if flat else np.zeros(0, bool)
+    packed = np.packbits(bits, bitorder="little")
+    # four spare bytes so that 32-bit reads of the last word stay in bounds
+    packed = np.concatenate([packed, np.zeros(4, np.uint8)])
+    return packed, np.asarray(offs, np.int64), dense
+
+
 def bf16_bits(t: torch.Tensor):
     """Raw bf16 bit patterns of a tensor as a CPU numpy uint16 array."""
     import numpy as np
