@@ -110,6 +110,32 @@ BIA_API int bia_prefill_paged(const bia_attn_desc *desc, const void *q, const vo
                       int32_t batch, int32_t causal, int32_t split_size, void *workspace,
                       size_t workspace_bytes, void *out, float *lse, void *stream);
 
+/*
+ * bia_prefill_paged with a custom attention mask: key j is visible to in-call
+ * token t of request b only if bit mask_indptr[b] + t*kv_len(b) + j of the
+ * mask is 1 (and, when causal, also j <= the token's position).  The mask is a
+ * little-endian bit string (bit k = (byte k/8 >> k%8) & 1), like the packed
+ * per-request [q_len, kv_len] masks of paged prefill wrappers; the pages name
+ * no custom mask, so this is the next-row extension of the same extend path
+ * ("sglang PR #43612", Summary: BatchPrefillWithPagedKVCacheWrapper).
+ *   mask:        device, 4-byte aligned, mask_bytes long; every request's
+ *                q_len*kv_len bits must lie in its first mask_bytes/4 words
+ *   mask_indptr: device int64 [batch+1] bit offsets (mask_indptr_host: the
+ *                host mirror, validated)
+ * A row that the mask leaves without keys gets out 0 and lse -inf.  The
+ * workspace is bia_prefill_workspace_size's.  Results for a request depend on
+ * its own mask bits, never on the batch.
+ */
+BIA_API int bia_prefill_paged_mask(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                           const void *v_cache, int64_t num_pages, const int32_t *qo_indptr,
+                           const int32_t *kv_indptr, const int32_t *kv_indices,
+                           const int32_t *kv_last_page_len, const int32_t *qo_indptr_host,
+                           const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                           int32_t batch, int32_t causal, int32_t split_size,
+                           const void *mask, size_t mask_bytes, const int64_t *mask_indptr,
+                           const int64_t *mask_indptr_host, void *workspace,
+                           size_t workspace_bytes, void *out, float *lse, void *stream);
+
 /* Workspace bytes bia_prefill_paged needs for this call (0 on invalid input). */
 BIA_API size_t bia_prefill_workspace_size(const bia_attn_desc *desc, const int32_t *qo_indptr_host,
                                   const int32_t *kv_indptr_host,

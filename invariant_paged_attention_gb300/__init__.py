@@ -33,7 +33,7 @@ EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged"
            "bia_decode_workspace_size", "bia_merge_states", "bia_q_tile_tokens",
            "bia_status_string", "bia_read_status", "bia_set_profile_events",
            "bia_launch_count", "bia_last_error", "bia_decode_paged_noalloc",
-           "bia_append_paged_kv")
+           "bia_append_paged_kv", "bia_prefill_paged_mask")
 
 
 class BiaError(RuntimeError):
@@ -95,6 +95,9 @@ def load(path: str = LIB_PATH):
     lib.bia_append_paged_kv.argtypes = [dp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                         vp, vp]
     lib.bia_append_paged_kv.restype = ctypes.c_int
+    lib.bia_prefill_paged_mask.argtypes = [dp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32,
+                                           i32, i32, vp, sz, vp, vp, vp, sz, vp, vp, vp]
+    lib.bia_prefill_paged_mask.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -157,6 +160,28 @@ def bia_prefill_paged(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indice
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
     if rc != BIA_OK:
         raise BiaError(rc, "bia_prefill_paged")
+
+
+def bia_prefill_paged_mask(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices,
+                           kv_last_page_len, qo_indptr_host, kv_indptr_host,
+                           kv_last_page_len_host, mask, mask_indptr, mask_indptr_host,
+                           workspace, out, lse=None, causal=True, split_size=0, stream=None):
+    """bia_prefill_paged with a custom mask: ``mask`` a device uint8 tensor of
+    little-endian bits, ``mask_indptr`` its device int64 [batch+1] bit
+    offsets (include/bia.h states the rule)."""
+    qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
+                     _host_i32(kv_last_page_len_host))
+    mih = torch.as_tensor(mask_indptr_host, dtype=torch.int64).contiguous()
+    if mih.device.type != "cpu":
+        raise ValueError("host mirrors must be CPU tensors")
+    rc = load().bia_prefill_paged_mask(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(qo),
+        _ptr(kvp), _ptr(last), len(qo) - 1, int(bool(causal)), int(split_size), _ptr(mask),
+        mask.numel() * mask.element_size(), _ptr(mask_indptr), _ptr(mih), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_prefill_paged_mask")
 
 
 def bia_decode_paged(desc, q, k_cache, v_cache, kv_indptr, kv_indices, kv_last_page_len,

@@ -150,13 +150,37 @@ float effective_scale(const bia_attn_desc *d) {
   return s * 1.4426950408889634f;
 }
 
+// Custom mask of a prefill call (bia_prefill_paged_mask).
+struct MaskArgs {
+  const void *bits;               // device, 4-byte aligned
+  size_t bytes;                   // size of the bit buffer
+  const int64_t *indptr;          // device [batch+1] bit offsets
+  const int64_t *indptr_host;     // host mirror
+};
+
+// Every request's [q_len, kv_len] bits lie inside the buffer's whole words.
+int check_mask(const MaskArgs &m, const int32_t *qo, const int32_t *kvp, const int32_t *last,
+               int32_t batch, int page_size) {
+  if (!m.bits || !m.indptr || !m.indptr_host) return BIA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(m.bits) & 3u) return BIA_ERR_INVALID_ARG;
+  const int64_t total_bits = static_cast<int64_t>(m.bytes / 4) * 32;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t q_len = static_cast<int64_t>(qo[b + 1]) - qo[b];
+    const int64_t pages = static_cast<int64_t>(kvp[b + 1]) - kvp[b];
+    const int64_t kv_len = pages > 0 ? (pages - 1) * page_size + last[b] : 0;
+    const int64_t off = m.indptr_host[b];
+    if (off < 0 || off > total_bits - q_len * kv_len) return BIA_ERR_INVALID_ARG;
+  }
+  return BIA_OK;
+}
+
 int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const void *k_cache,
                   const void *v_cache, int64_t num_pages, const int32_t *qo_indptr,
                   const int32_t *kv_indptr, const int32_t *kv_indices,
                   const int32_t *kv_last_page_len, const int32_t *qo_host,
                   const int32_t *kvp_host, const int32_t *last_host, int32_t batch,
                   int32_t causal, int32_t split, void *workspace, size_t workspace_bytes,
-                  void *out, float *lse, void *stream) {
+                  void *out, float *lse, void *stream, const MaskArgs *mask = nullptr) {
   int rc = check_desc(desc);
   if (rc != BIA_OK) return rc;
   if (!q || !k_cache || !v_cache || !kv_indptr || !kv_indices || !kv_last_page_len || !out ||
@@ -177,6 +201,10 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   rc = host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal, split,
                  tile_tokens, tiles_per_unit, ctas, &hp);
   if (rc != BIA_OK) return rc;
+  if (mask) {
+    rc = check_mask(*mask, qo_host, kvp_host, last_host, batch, desc->page_size);
+    if (rc != BIA_OK) return rc;
+  }
   const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows,
                                       desc->num_qo_heads, desc->head_dim);
   if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
@@ -238,6 +266,11 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   a.out = static_cast<uint16_t *>(out);
   a.lse = lse;
   a.status = pa.status;
+  if (mask) {
+    a.mask = static_cast<const uint32_t *>(mask->bits);
+    a.mask_indptr = mask->indptr;
+    a.mask_words = static_cast<int64_t>(mask->bytes / 4);
+  }
   if (!decode) {
     a.q_rows = static_cast<int32_t>(q_rows);
     a.kv_rows = static_cast<int32_t>(kv_rows);
@@ -296,6 +329,22 @@ int bia_prefill_paged(const bia_attn_desc *desc, const void *q, const void *k_ca
                        kv_indices, kv_last_page_len, qo_indptr_host, kv_indptr_host,
                        kv_last_page_len_host, batch, causal ? 1 : 0, split_size, workspace,
                        workspace_bytes, out, lse, stream);
+}
+
+int bia_prefill_paged_mask(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                           const void *v_cache, int64_t num_pages, const int32_t *qo_indptr,
+                           const int32_t *kv_indptr, const int32_t *kv_indices,
+                           const int32_t *kv_last_page_len, const int32_t *qo_indptr_host,
+                           const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                           int32_t batch, int32_t causal, int32_t split_size,
+                           const void *mask, size_t mask_bytes, const int64_t *mask_indptr,
+                           const int64_t *mask_indptr_host, void *workspace,
+                           size_t workspace_bytes, void *out, float *lse, void *stream) {
+  const MaskArgs m{mask, mask_bytes, mask_indptr, mask_indptr_host};
+  return run_attention(false, desc, q, k_cache, v_cache, num_pages, qo_indptr, kv_indptr,
+                       kv_indices, kv_last_page_len, qo_indptr_host, kv_indptr_host,
+                       kv_last_page_len_host, batch, causal ? 1 : 0, split_size, workspace,
+                       workspace_bytes, out, lse, stream, &m);
 }
 
 size_t bia_prefill_workspace_size(const bia_attn_desc *desc, const int32_t *qo_indptr_host,

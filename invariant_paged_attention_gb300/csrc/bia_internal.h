@@ -144,6 +144,11 @@ struct AttnArgs {
   // D] in 64-column boxes one row high; all SW128
   CUtensorMap tm_q, tm_k, tm_v;
   int32_t q_rows, kv_rows; // row extents of the maps (a row >= extent reads as zeros)
+  // optional custom mask (prefill): little-endian bit string of mask_words
+  // 32-bit words; request b's [q_len, kv_len] bits start at bit mask_indptr[b]
+  const uint32_t *mask;
+  const int64_t *mask_indptr;
+  int64_t mask_words;
 };
 
 // Paged-KV append: new token t of request b goes to position

@@ -76,10 +76,28 @@ struct TileInfo {
   bool has;           // the tile exists and touches this split
 };
 
-// Max of this thread's row of S (128 fp32 columns at taddr), over the first
-// n_vis columns unless FULL.  Two batches of 64 columns: two loads, one wait.
-template <bool FULL>
-__device__ __forceinline__ float row_block_max(uint32_t taddr, int32_t n_vis) {
+// Whether column c of the block is visible: bit c of the 128-bit set vis.
+__device__ __forceinline__ bool col_visible(const uint32_t (&vis)[4], int c) {
+  return (vis[c >> 5] >> (c & 31)) & 1u;
+}
+
+// Which columns of a block a row uses: kFull every column, kFirst the first
+// n_vis (causal / length limit), kBits the columns in a 128-bit set (custom
+// mask).
+enum ColMode { kFull, kFirst, kBits };
+
+template <int MODE>
+__device__ __forceinline__ bool col_used(int c, int32_t n_vis, const uint32_t (&vis)[4]) {
+  if constexpr (MODE == kFull) return true;
+  else if constexpr (MODE == kFirst) return c < n_vis;
+  else return col_visible(vis, c);
+}
+
+// Max of this thread's row of S (128 fp32 columns at taddr) over the columns
+// MODE selects.  Two batches of 64 columns: two loads, one wait.
+template <int MODE>
+__device__ __forceinline__ float row_block_max(uint32_t taddr, int32_t n_vis,
+                                               const uint32_t (&vis)[4]) {
   float bm = -INFINITY;
 #pragma unroll
   for (int h = 0; h < kKvBlock / 64; ++h) {
@@ -87,7 +105,7 @@ __device__ __forceinline__ float row_block_max(uint32_t taddr, int32_t n_vis) {
     tmem_ld32(taddr + h * 64, v0);
     tmem_ld32(taddr + h * 64 + 32, v1);
     tmem_wait_ld();
-    if constexpr (FULL) {
+    if constexpr (MODE == kFull) {
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
         bm = fmax3(bm, __uint_as_float(v0[i]), __uint_as_float(v0[i + 1]));
@@ -96,19 +114,20 @@ __device__ __forceinline__ float row_block_max(uint32_t taddr, int32_t n_vis) {
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        if (h * 64 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v0[i]));
-        if (h * 64 + 32 + i < n_vis) bm = fmaxf(bm, __uint_as_float(v1[i]));
+        if (col_used<MODE>(h * 64 + i, n_vis, vis)) bm = fmaxf(bm, __uint_as_float(v0[i]));
+        if (col_used<MODE>(h * 64 + 32 + i, n_vis, vis)) bm = fmaxf(bm, __uint_as_float(v1[i]));
       }
     }
   }
   return bm;
 }
 
-// P = 2^(s*scale - m_sub) of this thread's row (zero past n_vis unless FULL),
-// written as bf16 pairs over the first 64 columns of the same TMEM row;
-// returns the row sum of the fp32 P.
-template <bool FULL>
-__device__ __forceinline__ float row_block_p(uint32_t taddr, int32_t n_vis, float scale,
+// P = 2^(s*scale - m_sub) of this thread's row (zero in the columns MODE
+// leaves out), written as bf16 pairs over the first 64 columns of the same
+// TMEM row; returns the row sum of the fp32 P.
+template <int MODE>
+__device__ __forceinline__ float row_block_p(uint32_t taddr, int32_t n_vis,
+                                             const uint32_t (&vis)[4], float scale,
                                              float m_sub) {
   const uint64_t scale2 = f32x2(scale, scale);
   const uint64_t neg2 = f32x2(-m_sub, -m_sub);
@@ -125,9 +144,9 @@ __device__ __forceinline__ float row_block_p(uint32_t taddr, int32_t n_vis, floa
       f32x2_split(ffma2r(f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), scale2, neg2),
                   x0, x1);
       float p0 = ex2(x0), p1 = ex2(x1);
-      if constexpr (!FULL) {
-        if (c * 32 + i >= n_vis) p0 = 0.f;
-        if (c * 32 + i + 1 >= n_vis) p1 = 0.f;
+      if constexpr (MODE != kFull) {
+        if (!col_used<MODE>(c * 32 + i, n_vis, vis)) p0 = 0.f;
+        if (!col_used<MODE>(c * 32 + i + 1, n_vis, vis)) p1 = 0.f;
       }
       psum2 = fadd2(psum2, f32x2(p0, p1));
       pk[i / 2] = pack_bf16(p0, p1);
@@ -139,7 +158,7 @@ __device__ __forceinline__ float row_block_p(uint32_t taddr, int32_t n_vis, floa
   return ps0 + ps1;
 }
 
-template <int D>
+template <int D, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ AttnArgs a) {
   using L = Smem<D>;
   constexpr uint32_t kIdescS = idesc_bf16(128, kKvBlock, false);
@@ -340,20 +359,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const bool row_valid = me.has && t_row < r.q_len;
     const int32_t p_row = a.causal ? r.kv_len - r.q_len + t_row : r.kv_len - 1;
     const int32_t vis_last = min(p_row, r.kv_len - 1);
+    // custom mask (MASK): bit (mask_indptr[b] + t_row * kv_len + key) of the
+    // mask; rows past the request use none
+    constexpr bool use_mask = MASK;
+    const int64_t mask_row =
+        use_mask && row_valid ? a.mask_indptr[u.b] + static_cast<int64_t>(t_row) * r.kv_len : -1;
     float m = -INFINITY, l = 0.f; // running max (log2 units) and sum
     bool failed = false;
     for (int j = 0; j < me.n_blocks; ++j) {
+      const int32_t key0 = key_begin + j * kKvBlock;
+      const int32_t n_vis = vis_last - key0 + 1; // columns the causal / length rule allows
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if constexpr (use_mask) { // the row's 128 bits for this block (at any bit offset) AND n_vis
+        if (mask_row >= 0) {
+          const int64_t bit0 = mask_row + key0;
+          const int64_t w0 = bit0 >> 5;
+          const uint32_t sh = static_cast<uint32_t>(bit0 & 31);
+          uint32_t wd[5];
+#pragma unroll
+          for (int i = 0; i < 5; ++i) wd[i] = w0 + i < a.mask_words ? __ldg(a.mask + w0 + i) : 0u;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) vis[w] = __funnelshift_r(wd[w], wd[w + 1], sh);
+        }
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int n = min(max(n_vis - 32 * w, 0), 32);
+          vis[w] &= n >= 32 ? ~0u : ((1u << n) - 1u);
+        }
+      }
       if (!mbar_wait(bar(L::kSFull + t), j & 1, a.status)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      const int32_t key0 = key_begin + j * kKvBlock;
-      const int32_t n_vis = vis_last - key0 + 1; // visible columns of this block
-      // blocks every row of the warp sees in full skip the per-column mask
-      const bool full = __all_sync(0xffffffffu, n_vis >= kKvBlock);
+      // blocks every row of the warp sees in full skip the per-column test
+      const bool full = __all_sync(
+          0xffffffffu, use_mask ? (vis[0] & vis[1] & vis[2] & vis[3]) == ~0u : n_vis >= kKvBlock);
       const uint32_t srow = tS(t) + lane_base;
-      float bm = full ? row_block_max<true>(srow, n_vis) : row_block_max<false>(srow, n_vis);
+      float bm = full       ? row_block_max<kFull>(srow, n_vis, vis)
+                 : use_mask ? row_block_max<kBits>(srow, n_vis, vis)
+                            : row_block_max<kFirst>(srow, n_vis, vis);
       bm = bm == -INFINITY ? -INFINITY : bm * a.scale_log2;
       float m_use = m, alpha = 1.f;
       if (bm > m + kRescaleThreshold || (m == -INFINITY && bm != -INFINITY)) {
@@ -361,8 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         alpha = ex2(m - bm); // 0 when m == -inf
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      const float psum = full ? row_block_p<true>(srow, n_vis, a.scale_log2, m_sub)
-                              : row_block_p<false>(srow, n_vis, a.scale_log2, m_sub);
+      const float psum = full       ? row_block_p<kFull>(srow, n_vis, vis, a.scale_log2, m_sub)
+                         : use_mask ? row_block_p<kBits>(srow, n_vis, vis, a.scale_log2, m_sub)
+                                    : row_block_p<kFirst>(srow, n_vis, vis, a.scale_log2, m_sub);
       l = fmaf(l, alpha, psum);
       m = m_use;
       // rescale the running O row when the max moved (the previous P.V has
@@ -488,12 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
 }
 
-template <int D>
+template <int D, bool MASK>
 cudaError_t launch_prefill_d(const AttnArgs &a, cudaStream_t s) {
   using L = Smem<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MASK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
@@ -510,7 +556,7 @@ cudaError_t launch_prefill_d(const AttnArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel<D>, a);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<D, MASK>, a);
 }
 
 } // namespace
@@ -518,7 +564,9 @@ cudaError_t launch_prefill_d(const AttnArgs &a, cudaStream_t s) {
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
   if (a.n_units % kCtas != 0) return cudaErrorInvalidValue; // the planner pairs every unit
-  return a.D == 128 ? launch_prefill_d<128>(a, s) : launch_prefill_d<64>(a, s);
+  if (a.mask)
+    return a.D == 128 ? launch_prefill_d<128, true>(a, s) : launch_prefill_d<64, true>(a, s);
+  return a.D == 128 ? launch_prefill_d<128, false>(a, s) : launch_prefill_d<64, false>(a, s);
 }
 
 } // namespace bia
