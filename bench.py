@@ -408,6 +408,16 @@ def run_sweep(args):
     cm, km = time_calls([prefill_fn(pst, pc)])
     emit("cfg5 mixed prefill call (4096-tok chunk + 64 one-token extends, page 16)", "prefill",
          prefill_flops(pc, D, Hq), cm, km, {"kv_bytes": kv_bytes(pc, Hkv, D)})
+    # its two parts on their own: the chunk (tensor bound) and the one-token
+    # extends (K/V streaming through the prefill kernel)
+    chunk = wl.make_call(pst, [(0, 0, pst.seqs[0].new)])
+    cm, km = time_calls([prefill_fn(pst, chunk)])
+    emit("cfg5 chunk alone (4096 new tokens after a 4096-token prefix, page 16)", "prefill",
+         prefill_flops(chunk, D, Hq), cm, km)
+    ext = wl.make_call(pst, [(i, 0, 1) for i in range(1, len(pst.seqs))])
+    cm, km = time_calls([prefill_fn(pst, ext)])
+    emit("cfg5 one-token extends alone (64, ctx U[1024,32768], page 16)", "kv-stream",
+         kv_bytes(ext, Hkv, D), cm, km)
     dc = wl.whole_prefill(dst)
     cm, km = time_calls([decode_fn(dst, dc)])
     emit("cfg5 decodes (32 x 131072 ctx, page 16)", "decode", kv_bytes(dc, Hkv, D), cm, km)

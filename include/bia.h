@@ -46,7 +46,8 @@
  * outside [0, num_pages) is caught on the device: the row is read as zeros and
  * bit 0 of the workspace status word is set (bia_read_status).
  *
- * Supported: head_dim 64 or 128; num_qo_heads / num_kv_heads in {1,2,4,8};
+ * Supported: head_dim 64, 96 or 128 (96 runs zero-padded on the 128 kernels);
+ * num_qo_heads / num_kv_heads in {1,2,4,8};
  * page_size a power of two in 1..256; split sizes positive multiples of 128.
  */
 #ifndef BIA_H
@@ -83,7 +84,7 @@ typedef enum bia_status {
 typedef struct bia_attn_desc {
     int32_t num_qo_heads;
     int32_t num_kv_heads;
-    int32_t head_dim;  /* 64 or 128 */
+    int32_t head_dim;  /* 64, 96 or 128 */
     int32_t page_size; /* power of two, 1..256 */
     float sm_scale;    /* <= 0: 1/sqrt(head_dim) */
 } bia_attn_desc;

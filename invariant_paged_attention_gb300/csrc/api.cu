@@ -53,7 +53,7 @@ int check_desc(const bia_attn_desc *d) {
   if (d->num_qo_heads % d->num_kv_heads != 0) return BIA_ERR_UNSUPPORTED;
   const int G = d->num_qo_heads / d->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return BIA_ERR_UNSUPPORTED;
-  if (d->head_dim != 64 && d->head_dim != 128) return BIA_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128) return BIA_ERR_UNSUPPORTED;
   if (!is_pow2(d->page_size) || d->page_size > 256) return BIA_ERR_UNSUPPORTED;
   if (!(std::isfinite(d->sm_scale))) return BIA_ERR_INVALID_ARG;
   return BIA_OK;

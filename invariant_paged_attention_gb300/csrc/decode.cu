@@ -138,6 +138,15 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     for (int s = 0; s < NS; ++s) mbar_init(bar(s), 1);
     fence_mbar_init();
   }
+  // head_dim Dr < D (96 on the 128-wide layout): rows are copied Dr*2 bytes
+  // into D*2-byte slots whose tails stay zero, and the q lanes past Dr hold 0
+  const int Dr = a.D;
+  const uint32_t row_copy = static_cast<uint32_t>(Dr) * 2;
+  if (Dr < D) {
+    for (int b = lane * 16; b < L::kRing; b += 32 * 16)
+      asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(ring + b), "r"(0) : "memory");
+    fence_proxy_async(); // the zeros precede the ring's bulk copies
+  }
   __syncwarp();
 
   // ---- chunk loads: lanes 0..7 copy key rows, 8..15 the value rows of the
@@ -168,12 +177,12 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     }
     const int n_ok = __popc(__ballot_sync(0xffffffffu, ok));
     __syncwarp();
-    if (lane == 0) mbar_expect_tx(bar(st), static_cast<uint32_t>(n_ok) * L::kRow);
+    if (lane == 0) mbar_expect_tx(bar(st), static_cast<uint32_t>(n_ok) * row_copy);
     __syncwarp();
     if (ok) {
       const int64_t off =
-          (((static_cast<int64_t>(pg) << a.page_shift) + (key & page_mask)) * a.Hkv + kvh) * D;
-      bulk_g2s(dst, (lane < 8 ? a.k_cache : a.v_cache) + off, L::kRow, bar(st));
+          (((static_cast<int64_t>(pg) << a.page_shift) + (key & page_mask)) * a.Hkv + kvh) * Dr;
+      bulk_g2s(dst, (lane < 8 ? a.k_cache : a.v_cache) + off, row_copy, bar(st));
     }
   };
   for (int i = 0; i < NS && i < my_chunks; ++i) issue(i);
@@ -182,8 +191,9 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
   uint64_t q2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const uint4 w = *reinterpret_cast<const uint4 *>(
-        a.q + (static_cast<int64_t>(r.q_start) * a.Hq + kvh * G + g) * D + sub * 8);
+    const uint4 w = sub * 8 < Dr ? *reinterpret_cast<const uint4 *>(
+        a.q + (static_cast<int64_t>(r.q_start) * a.Hq + kvh * G + g) * Dr + sub * 8)
+                                 : make_uint4(0u, 0u, 0u, 0u);
     const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2);
     q2[g][0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
     q2[g][1] = fmul2(bf16x2_to_f32x2(w.y), sc2);
@@ -341,6 +351,7 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
   const bool single = (r.kv_len - 1) / a.split == 0; // one split: the final row
   for (int e = threadIdx.x; e < G * D; e += kThreadsDec) {
     const int g = e / D, d = e % D;
+    if (d >= Dr) continue;
     float M = -INFINITY;
 #pragma unroll
     for (int k = 0; k < kWarps; ++k) M = fmaxf(M, s_m[k * G + g]);
@@ -359,11 +370,11 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     const float lse = empty_row ? -INFINITY : __fmul_rn(__fadd_rn(M, lg2(Ls)), kLn2);
     const int64_t row = static_cast<int64_t>(r.q_start) * a.Hq + h;
     if (single) {
-      a.out[row * D + d] = to_bf16(val);
+      a.out[row * Dr + d] = to_bf16(val);
       if (a.lse && d == 0) a.lse[row] = lse;
     } else {
       const int64_t prow = (r.rowbase + u.split) * a.Hq + h;
-      a.part_o[prow * D + d] = val;
+      a.part_o[prow * Dr + d] = val;
       if (d == 0) a.part_lse[prow] = lse;
     }
   }
@@ -400,7 +411,8 @@ cudaError_t launch_decode_d(const AttnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
-  return a.D == 128 ? launch_decode_d<128>(a, s) : launch_decode_d<64>(a, s);
+  // head_dim 96 runs on the 128-wide layout, zero-padded
+  return a.D > 64 ? launch_decode_d<128>(a, s) : launch_decode_d<64>(a, s);
 }
 
 } // namespace bia

@@ -455,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       };
       uint8_t *stage = smem + L::kQ0 + t * L::kTile; // 128 rows x D*2 bytes
       constexpr int row_bytes = D * 2;
+      const int Dr = a.D; // head_dim 96 runs on the 128-wide layout, zero-padded
       constexpr int chunks = row_bytes / 16; // 16-byte chunks per staged row
       const int pass_cols = final_row ? D : D / 2;
       const int n_pass = D / pass_cols;
@@ -505,13 +506,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int r0 = 0; r0 < kTileRows; r0 += rows_per_step) {
           const int rr = r0 + tl / chunks, c = tl % chunks;
           const int32_t t_rr = me.tile * T + (rr >> gs);
-          if (t_rr < r.q_len) {
+          // 16-byte chunks of real columns: 8 bf16 or 4 fp32 each
+          const int c_lim = final_row ? Dr / 8 : min(pass_cols, Dr - ps * pass_cols) / 4;
+          if (t_rr < r.q_len && c < c_lim) {
             const uint4 w =
                 reinterpret_cast<const uint4 *>(stage + rr * row_bytes)[c ^ (rr % chunks)];
             if (final_row)
-              reinterpret_cast<uint4 *>(a.out + out_row_of(rr) * D)[c] = w;
+              reinterpret_cast<uint4 *>(a.out + out_row_of(rr) * Dr)[c] = w;
             else
-              reinterpret_cast<uint4 *>(a.part_o + part_row_of(rr) * D + ps * pass_cols)[c] = w;
+              reinterpret_cast<uint4 *>(a.part_o + part_row_of(rr) * Dr + ps * pass_cols)[c] = w;
           }
         }
         bar_sync_named(1 + t, 128); // the stage is rewritten by the next pass
@@ -564,9 +567,11 @@ cudaError_t launch_prefill_d(const AttnArgs &a, cudaStream_t s) {
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
   if (a.n_units % kCtas != 0) return cudaErrorInvalidValue; // the planner pairs every unit
+  // head_dim 96 runs on the 128-wide layout: the tensor maps read columns
+  // 96..127 as zeros, so S and the first 96 columns of O are unchanged
   if (a.mask)
-    return a.D == 128 ? launch_prefill_d<128, true>(a, s) : launch_prefill_d<64, true>(a, s);
-  return a.D == 128 ? launch_prefill_d<128, false>(a, s) : launch_prefill_d<64, false>(a, s);
+    return a.D > 64 ? launch_prefill_d<128, true>(a, s) : launch_prefill_d<64, true>(a, s);
+  return a.D > 64 ? launch_prefill_d<128, false>(a, s) : launch_prefill_d<64, false>(a, s);
 }
 
 } // namespace bia

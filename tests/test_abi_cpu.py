@@ -81,7 +81,7 @@ def test_workspace_size_counts_split_partials(bia):
     assert two_splits - one_split >= 5000 * 2 * 32 * 129 * 4
     # bad inputs answer 0
     assert bia.bia_prefill_workspace_size(desc, qo, kvp, last, True, 100) == 0
-    assert bia.bia_prefill_workspace_size(bia.make_desc(32, 8, 96, 1), qo, kvp, last) == 0
+    assert bia.bia_prefill_workspace_size(bia.make_desc(32, 8, 80, 1), qo, kvp, last) == 0
     assert bia.bia_decode_workspace_size(desc, kvp, last) > 0
 
 
@@ -109,7 +109,7 @@ def test_prefill_rejects_bad_arguments_on_the_host(bia):
     assert call_prefill(bia, d, [0, 10], [0, 5], [1]) == inv  # q_len > kv_len (causal)
     assert call_prefill(bia, d, [0, 10], [0, 10], [0]) == inv  # last page length 0
     assert call_prefill(bia, d, [0, 10], [0, 10], [1], split=100) == uns
-    assert call_prefill(bia, bia.make_desc(32, 8, 96, 1), [0, 10], [0, 10], [1]) == uns
+    assert call_prefill(bia, bia.make_desc(32, 8, 80, 1), [0, 10], [0, 10], [1]) == uns
     assert call_prefill(bia, bia.make_desc(32, 6, 128, 1), [0, 10], [0, 10], [1]) == uns
     assert call_prefill(bia, bia.make_desc(48, 3, 128, 1), [0, 10], [0, 10], [1]) == uns
     assert call_prefill(bia, bia.make_desc(32, 8, 128, 3), [0, 10], [0, 10], [1]) == uns

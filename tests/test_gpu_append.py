@@ -31,7 +31,8 @@ def _oracle_append(call, kc, vc, k_new, v_new):
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,P,chunk", [(32, 8, 128, 1, 300), (32, 8, 128, 16, 64),
-                                              (16, 2, 64, 64, 100), (8, 8, 128, 256, 1000)])
+                                              (16, 2, 64, 64, 100), (8, 8, 128, 256, 1000),
+                                              (32, 8, 96, 16, 64)])
 def test_append_matches_oracle_bitwise(Hq, Hkv, D, P, chunk):
     store = wl.PagedStore([wl.Sequence(700 + i, pre, new) for i, (pre, new) in
                            enumerate([(0, 1000), (3000, 77), (5, 0), (129, 640), (0, 1)])],
@@ -119,7 +120,7 @@ def test_host_validation():
                                 *args[1:], too_many, call.kv_indptr, call.kv_last_page_len)
     assert e.value.status == bia.BIA_ERR_INVALID_ARG
     with pytest.raises(bia.BiaError) as e:
-        bia.bia_append_paged_kv(bia.make_desc(4, 1, 96, 16), k_new, v_new, store.k_cache,
+        bia.bia_append_paged_kv(bia.make_desc(4, 1, 80, 16), k_new, v_new, store.k_cache,
                                 store.v_cache, *args, call.qo_indptr, call.kv_indptr,
                                 call.kv_last_page_len)
     assert e.value.status == bia.BIA_ERR_UNSUPPORTED

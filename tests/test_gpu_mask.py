@@ -62,6 +62,7 @@ def check(call, out, lse, ref_out, ref_lse):
 SHAPES = [  # (Hq, Hkv, D, P, [(prefix, new)])
     (32, 8, 128, 16, [(0, 300), (700, 77), (5, 1), (0, 0), (129, 160)]),
     (4, 1, 64, 1, [(0, 256), (33, 100)]),
+    (32, 8, 96, 16, [(0, 130), (4090, 20)]),
 ]
 
 
