@@ -53,7 +53,8 @@ int check_desc(const bia_attn_desc *d) {
   if (d->num_qo_heads % d->num_kv_heads != 0) return BIA_ERR_UNSUPPORTED;
   const int G = d->num_qo_heads / d->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return BIA_ERR_UNSUPPORTED;
-  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128) return BIA_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128 && d->head_dim != 256)
+    return BIA_ERR_UNSUPPORTED;
   if (!is_pow2(d->page_size) || d->page_size > 256) return BIA_ERR_UNSUPPORTED;
   if (!(std::isfinite(d->sm_scale))) return BIA_ERR_INVALID_ARG;
   return BIA_OK;
@@ -194,7 +195,7 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
   const int G = desc->num_qo_heads / desc->num_kv_heads;
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
-  const int tiles_per_unit = decode ? 1 : bia::kPrefillTilesPerUnit;
+  const int tiles_per_unit = decode ? 1 : bia::prefill_tiles_per_unit(desc->head_dim);
   const int ctas = decode ? 1 : bia::kPrefillClusterCtas;
   if (decode) causal = 1;
   HostPlan hp;
@@ -283,7 +284,9 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
 
   const bool profile = g_attn_begin != nullptr && g_attn_end != nullptr;
   if (profile && cudaEventRecord(g_attn_begin, st) != cudaSuccess) return BIA_ERR_CUDA;
-  cudaError_t e = decode ? bia::launch_decode(a, st) : bia::launch_prefill(a, st);
+  cudaError_t e = decode                     ? bia::launch_decode(a, st)
+                  : desc->head_dim == 256 ? bia::launch_prefill_wide(a, st)
+                                          : bia::launch_prefill(a, st);
   if (e != cudaSuccess) return cuda_fail(decode ? "decode kernel launch" : "prefill kernel launch", e);
   if (hp.n_units > 0) __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   if (profile && cudaEventRecord(g_attn_end, st) != cudaSuccess) return BIA_ERR_CUDA;
@@ -303,7 +306,7 @@ size_t workspace_size(bool decode, const bia_attn_desc *desc, const int32_t *qo_
   if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
   const int G = desc->num_qo_heads / desc->num_kv_heads;
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
-  const int tiles_per_unit = decode ? 1 : bia::kPrefillTilesPerUnit;
+  const int tiles_per_unit = decode ? 1 : bia::prefill_tiles_per_unit(desc->head_dim);
   const int ctas = decode ? 1 : bia::kPrefillClusterCtas;
   HostPlan hp;
   if (host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, decode ? 1 : causal,

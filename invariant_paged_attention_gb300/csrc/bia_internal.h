@@ -19,6 +19,10 @@ constexpr int32_t kStatusTimeout = 4;      // a bounded device wait gave up
 constexpr int kTileRows = 128; // q tile rows (GQA-packed)
 constexpr int kKvBlock = 128;  // keys per block of the prefill inner loop
 constexpr int kPrefillTilesPerUnit = 2; // q tiles sharing one K/V stream in a prefill CTA
+// q tiles per prefill CTA for a head dim: one for 256 (its O fills half of TMEM)
+inline int prefill_tiles_per_unit(int head_dim) {
+  return head_dim == 256 ? 1 : kPrefillTilesPerUnit;
+}
 constexpr int kPrefillClusterCtas = 4;  // prefill CTAs of a cluster sharing each K/V gather
 
 // Per-request record written by the plan kernel.
@@ -166,6 +170,7 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_wide(const AttnArgs &a, cudaStream_t s); // head_dim 256
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_merge_states(const float *v, const float *s, const int32_t *num_states,
                                 int64_t n, int32_t S, int32_t H, int32_t D, uint16_t *out,

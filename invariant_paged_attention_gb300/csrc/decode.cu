@@ -32,7 +32,7 @@ constexpr float kLazyThreshold = 8.0f; // log2 units
 
 template <int D>
 struct DecSmem {
-  static constexpr int kStages = D == 128 ? 3 : 5;
+  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 3 : 5);
   static constexpr int kRow = D * 2;                  // bytes of one key row
   static constexpr int kStage = 2 * kChunk * kRow;    // K rows then V rows
   static constexpr int kRing = kStages * kStage;      // one warp's ring
@@ -412,6 +412,7 @@ cudaError_t launch_decode_d(const AttnArgs &a, cudaStream_t s) {
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
   // head_dim 96 runs on the 128-wide layout, zero-padded
+  if (a.D == 256) return launch_decode_d<256>(a, s);
   return a.D > 64 ? launch_decode_d<128>(a, s) : launch_decode_d<64>(a, s);
 }
 

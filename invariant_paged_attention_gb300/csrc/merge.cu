@@ -145,7 +145,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t st) {
   if (a.total_rows == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(a.total_rows);
-  merge_partials_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(a);
+  if (a.D <= 128)
+    merge_partials_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(a);
+  else // head_dim 256: eight floats per lane
+    merge_partials_kernel<8><<<grid, kMergeWarps * 32, 0, st>>>(a);
   return cudaGetLastError();
 }
 

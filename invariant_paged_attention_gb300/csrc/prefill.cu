@@ -42,6 +42,7 @@
 // kernel folds in split order.
 #include "bia_internal.h"
 #include "ptx.cuh"
+#include "softmax_rows.cuh"
 
 namespace bia {
 
@@ -75,88 +76,6 @@ struct TileInfo {
   int32_t n_blocks;   // 128-key blocks of this unit's split it needs
   bool has;           // the tile exists and touches this split
 };
-
-// Whether column c of the block is visible: bit c of the 128-bit set vis.
-__device__ __forceinline__ bool col_visible(const uint32_t (&vis)[4], int c) {
-  return (vis[c >> 5] >> (c & 31)) & 1u;
-}
-
-// Which columns of a block a row uses: kFull every column, kFirst the first
-// n_vis (causal / length limit), kBits the columns in a 128-bit set (custom
-// mask).
-enum ColMode { kFull, kFirst, kBits };
-
-template <int MODE>
-__device__ __forceinline__ bool col_used(int c, int32_t n_vis, const uint32_t (&vis)[4]) {
-  if constexpr (MODE == kFull) return true;
-  else if constexpr (MODE == kFirst) return c < n_vis;
-  else return col_visible(vis, c);
-}
-
-// Max of this thread's row of S (128 fp32 columns at taddr) over the columns
-// MODE selects.  Two batches of 64 columns: two loads, one wait.
-template <int MODE>
-__device__ __forceinline__ float row_block_max(uint32_t taddr, int32_t n_vis,
-                                               const uint32_t (&vis)[4]) {
-  float bm = -INFINITY;
-#pragma unroll
-  for (int h = 0; h < kKvBlock / 64; ++h) {
-    uint32_t v0[32], v1[32];
-    tmem_ld32(taddr + h * 64, v0);
-    tmem_ld32(taddr + h * 64 + 32, v1);
-    tmem_wait_ld();
-    if constexpr (MODE == kFull) {
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        bm = fmax3(bm, __uint_as_float(v0[i]), __uint_as_float(v0[i + 1]));
-        bm = fmax3(bm, __uint_as_float(v1[i]), __uint_as_float(v1[i + 1]));
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (col_used<MODE>(h * 64 + i, n_vis, vis)) bm = fmaxf(bm, __uint_as_float(v0[i]));
-        if (col_used<MODE>(h * 64 + 32 + i, n_vis, vis)) bm = fmaxf(bm, __uint_as_float(v1[i]));
-      }
-    }
-  }
-  return bm;
-}
-
-// P = 2^(s*scale - m_sub) of this thread's row (zero in the columns MODE
-// leaves out), written as bf16 pairs over the first 64 columns of the same
-// TMEM row; returns the row sum of the fp32 P.
-template <int MODE>
-__device__ __forceinline__ float row_block_p(uint32_t taddr, int32_t n_vis,
-                                             const uint32_t (&vis)[4], float scale,
-                                             float m_sub) {
-  const uint64_t scale2 = f32x2(scale, scale);
-  const uint64_t neg2 = f32x2(-m_sub, -m_sub);
-  uint64_t psum2 = 0;
-#pragma unroll
-  for (int c = 0; c < kKvBlock / 32; ++c) {
-    uint32_t v[32];
-    tmem_ld32(taddr + c * 32, v);
-    tmem_wait_ld();
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      float x0, x1;
-      f32x2_split(ffma2r(f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), scale2, neg2),
-                  x0, x1);
-      float p0 = ex2(x0), p1 = ex2(x1);
-      if constexpr (MODE != kFull) {
-        if (!col_used<MODE>(c * 32 + i, n_vis, vis)) p0 = 0.f;
-        if (!col_used<MODE>(c * 32 + i + 1, n_vis, vis)) p1 = 0.f;
-      }
-      psum2 = fadd2(psum2, f32x2(p0, p1));
-      pk[i / 2] = pack_bf16(p0, p1);
-    }
-    tmem_st16(taddr + c * 16, pk);
-  }
-  float ps0, ps1;
-  f32x2_split(psum2, ps0, ps1);
-  return ps0 + ps1;
-}
 
 template <int D, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ AttnArgs a) {
@@ -396,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const bool full = __all_sync(
           0xffffffffu, use_mask ? (vis[0] & vis[1] & vis[2] & vis[3]) == ~0u : n_vis >= kKvBlock);
       const uint32_t srow = tS(t) + lane_base;
-      float bm = full       ? row_block_max<kFull>(srow, n_vis, vis)
-                 : use_mask ? row_block_max<kBits>(srow, n_vis, vis)
-                            : row_block_max<kFirst>(srow, n_vis, vis);
+      float bm = full       ? row_block_max<kKvBlock, kFull>(srow, n_vis, vis)
+                 : use_mask ? row_block_max<kKvBlock, kBits>(srow, n_vis, vis)
+                            : row_block_max<kKvBlock, kFirst>(srow, n_vis, vis);
       bm = bm == -INFINITY ? -INFINITY : bm * a.scale_log2;
       float m_use = m, alpha = 1.f;
       if (bm > m + kRescaleThreshold || (m == -INFINITY && bm != -INFINITY)) {
@@ -406,9 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         alpha = ex2(m - bm); // 0 when m == -inf
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      const float psum = full       ? row_block_p<kFull>(srow, n_vis, vis, a.scale_log2, m_sub)
-                         : use_mask ? row_block_p<kBits>(srow, n_vis, vis, a.scale_log2, m_sub)
-                                    : row_block_p<kFirst>(srow, n_vis, vis, a.scale_log2, m_sub);
+      const float psum = full       ? row_block_p<kKvBlock, kFull>(srow, n_vis, vis, a.scale_log2, m_sub)
+                         : use_mask ? row_block_p<kKvBlock, kBits>(srow, n_vis, vis, a.scale_log2, m_sub)
+                                    : row_block_p<kKvBlock, kFirst>(srow, n_vis, vis, a.scale_log2, m_sub);
       l = fmaf(l, alpha, psum);
       m = m_use;
       // rescale the running O row when the max moved (the previous P.V has

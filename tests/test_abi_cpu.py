@@ -157,7 +157,7 @@ def test_append_rejects_bad_arguments_on_the_host(bia):
     assert call(d, [0, 1], [0, 1], [0]) == inv  # last page length 0
     assert call(d, [0, 1], [0, 1], [1], k_new=FAKE + 8) == inv  # unaligned rows
     assert call(d, [0, 1], [0, 1], [1], status=FAKE + 2) == inv  # unaligned status word
-    assert call(bia.make_desc(32, 8, 256, 16), [0, 1], [0, 1], [1]) == bia.BIA_ERR_UNSUPPORTED
+    assert call(bia.make_desc(32, 8, 80, 16), [0, 1], [0, 1], [1]) == bia.BIA_ERR_UNSUPPORTED
     # nothing to write and no status word: returns before touching the device
     assert call(d, [0, 0, 0], [0, 1, 3], [5, 2]) == bia.BIA_OK
 

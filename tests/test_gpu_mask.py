@@ -63,6 +63,7 @@ SHAPES = [  # (Hq, Hkv, D, P, [(prefix, new)])
     (32, 8, 128, 16, [(0, 300), (700, 77), (5, 1), (0, 0), (129, 160)]),
     (4, 1, 64, 1, [(0, 256), (33, 100)]),
     (32, 8, 96, 16, [(0, 130), (4090, 20)]),
+    (16, 8, 256, 16, [(0, 200), (4090, 30)]),
 ]
 
 
