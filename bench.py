@@ -423,6 +423,20 @@ def run_sweep(args):
     emit("cfg5 decodes (32 x 131072 ctx, page 16)", "decode", kv_bytes(dc, Hkv, D), cm, km)
     del pst, dst, pc, dc
     torch.cuda.empty_cache()
+    # head_dim 256 (16 q / 8 kv heads): the wide prefill kernel and decode
+    st = wl.wide_prefill(dev)
+    c = wl.whole_prefill(st)
+    cm, km = time_calls([prefill_fn(st, c)])
+    emit("head_dim 256 prefill (cfg2 lengths, 16q/8kv, page 1)", "prefill",
+         prefill_flops(c, 256, 16), cm, km)
+    del st, c
+    st = wl.wide_decode(dev, 64)
+    c = wl.whole_prefill(st)
+    cm, km = time_calls([decode_fn(st, c)])
+    emit("head_dim 256 decode B=64 (ctx U[1024,32768], 16q/8kv, page 1)", "decode",
+         kv_bytes(c, 8, 256), cm, km)
+    del st, c
+    torch.cuda.empty_cache()
     for B in (1, 8, 64, 256):
         st = wl.cfg4_decode(dev, B)
         c = wl.whole_prefill(st)

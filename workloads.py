@@ -270,6 +270,22 @@ def cfg4_decode(device, batch: int, lo: int = 1024, hi: int = 32768) -> PagedSto
     return PagedStore(seqs, page_size=1, device=device, layout_seed=4999 + batch, **QWEN)
 
 
+def wide_prefill(device, batch: int = 8) -> PagedStore:
+    """cfg2's lengths (uniform in [512, 8192], same seed) with head_dim 256:
+    16 q heads / 8 kv heads (a Gemma-style layout), page 1."""
+    lens = uniform_lengths(batch, 512, 8192, 2000)
+    seqs = [Sequence(7000 + i, 0, L) for i, L in enumerate(lens)]
+    return PagedStore(seqs, 16, 8, 256, 1, device, layout_seed=7999)
+
+
+def wide_decode(device, B: int = 64) -> PagedStore:
+    """cfg4-style decode (contexts uniform in [1024, 32768]) at head_dim 256,
+    16 q heads / 8 kv heads, page 1."""
+    ctx = uniform_lengths(B, 1024, 32768, 4000)
+    seqs = [Sequence(7500 + i, c - 1, 1) for i, c in enumerate(ctx)]
+    return PagedStore(seqs, 16, 8, 256, 1, device, layout_seed=7998)
+
+
 def cfg5_mixed(device, n_extend: int = 64, n_decode: int = 32, decode_ctx: int = 131072,
                chunk: int = 4096, chunk_prefix: int = 4096):
     """Mixed serving batch, page 16: one prefill chunk (prefix 4096 + 4096 new),
