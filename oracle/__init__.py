@@ -56,6 +56,9 @@ def _load():
                                                          vp, vp, vp, vp, vp, i32, i64, i64, vp,
                                                          vp, vp, i64, vp, vp, i32]
             lib.oracle_attention_rows_masked.restype = i32
+            lib.oracle_mla.argtypes = [i32, i32, i32, i32, f64, i32, vp, vp, vp, vp, vp, vp, vp,
+                                       vp, i32, i64, i64, vp, vp]
+            lib.oracle_mla.restype = i32
             lib.oracle_row_probs.argtypes = [i32, i32, i32, i32, f64, i32, vp, vp, vp, vp, vp,
                                              vp, vp, i32, i64, i32, vp, i64]
             lib.oracle_row_probs.restype = i32
@@ -211,3 +214,30 @@ def append_paged_kv(k_cache, v_cache, k_new, v_new, append_indptr, kv_indptr, kv
             kc[page, p % page_size] = kn[ap[b] + i]
             vc[page, p % page_size] = vn[ap[b] + i]
     return kc, vc
+
+
+def mla(q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len,
+        *, page_size, sm_scale, causal=True, key_window=None):
+    """Multi-head latent attention over a paged latent cache, fp64: every q
+    head attends to the shared rows [ckv | kpe] with scores
+    sm_scale * (<q_nope, ckv> + <q_pe, kpe>) and takes the ckv rows as values.
+    q_nope [total_q, H, Dc], q_pe [total_q, H, Dp], ckv_cache
+    [num_pages, P, Dc], kpe_cache [num_pages, P, Dp] as bf16 bit patterns.
+    Returns (out [total_q, H, Dc], lse [total_q, H]) float64."""
+    lib = _load()
+    qn, qp = _u16(q_nope), _u16(q_pe)
+    ckv, kpe = _u16(ckv_cache), _u16(kpe_cache)
+    qo, kvp, kvi, last = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(kv_last_page_len)
+    if kvi.size == 0:
+        kvi = np.zeros(1, np.int32)
+    total_q, H, dc = qn.shape
+    dp = qp.shape[2]
+    lo, hi = (0, np.iinfo(np.int64).max) if key_window is None else key_window
+    out = np.zeros((max(total_q, 1), H, dc), np.float64)
+    lse = np.zeros((max(total_q, 1), H), np.float64)
+    rc = lib.oracle_mla(H, dc, dp, page_size, float(sm_scale), int(bool(causal)), _ptr(qn),
+                        _ptr(qp), _ptr(ckv), _ptr(kpe), _ptr(qo), _ptr(kvp), _ptr(kvi), _ptr(last),
+                        len(qo) - 1, int(lo), int(hi), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_mla failed with {rc}")
+    return out[:total_q], lse[:total_q]

@@ -401,3 +401,101 @@ int oracle_merge_states(const float *v, const float *lse_in, const int32_t *num_
     }
     return ORACLE_OK;
 }
+
+/*
+ * Multi-head latent attention (MLA) over a paged latent cache, by its
+ * definition.  The pages name the paged MLA wrapper their serving stack uses
+ * for chunked extends of Kimi-Linear and note that it has no deterministic
+ * mode ("sglang PR #43612", Summary); what it computes, in the absorbed form
+ * paged MLA kernels take, is plain attention of every q head over one shared
+ * latent cache:
+ *   s_j = sm_scale * (<q_nope, ckv_j> + <q_pe, kpe_j>),
+ *   out = sum_j softmax(s)_j * ckv_j   (the latent row doubles as the value),
+ *   lse = m + ln sum_j e^{s_j - m}.
+ * Token t of request b sits at position kv_len - q_len + t and, causal, sees
+ * keys 0..that position.  q_nope [total_q, H, Dc], q_pe [total_q, H, Dp],
+ * ckv_cache [num_pages, P, Dc], kpe_cache [num_pages, P, Dp] (bf16 bits);
+ * out [total_q, H, Dc] fp64, lse [total_q, H] fp64.  key_lo / key_hi bound the
+ * visible keys (a split partial).
+ */
+int oracle_mla(int32_t num_heads, int32_t dc, int32_t dp, int32_t page_size, double sm_scale,
+               int32_t causal, const uint16_t *q_nope, const uint16_t *q_pe,
+               const uint16_t *ckv_cache, const uint16_t *kpe_cache, const int32_t *qo_indptr,
+               const int32_t *kv_indptr, const int32_t *kv_indices,
+               const int32_t *kv_last_page_len, int32_t batch, int64_t key_lo, int64_t key_hi,
+               double *out, double *lse)
+{
+    if (num_heads <= 0 || dc <= 0 || dp < 0 || page_size <= 0 || batch <= 0 || !q_nope ||
+        (dp > 0 && (!q_pe || !kpe_cache)) || !ckv_cache || !qo_indptr || !kv_indptr ||
+        !kv_indices || !kv_last_page_len || !out || !lse)
+        return ORACLE_BAD_ARG;
+    int64_t max_kv = 1;
+    for (int b = 0; b < batch; b++) {
+        int64_t pages = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+        int64_t kv = pages > 0 ? (pages - 1) * page_size + kv_last_page_len[b] : 0;
+        if (kv > max_kv)
+            max_kv = kv;
+    }
+    double *scores = (double *)malloc((size_t)max_kv * sizeof(double));
+    if (!scores)
+        return ORACLE_NO_MEM;
+    for (int b = 0; b < batch; b++) {
+        int64_t pages = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+        int64_t kv_len = pages > 0 ? (pages - 1) * page_size + kv_last_page_len[b] : 0;
+        int64_t q_len = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+        for (int64_t tl = 0; tl < q_len; tl++) {
+            int64_t t = qo_indptr[b] + tl;
+            int64_t p = kv_len - q_len + tl;
+            int64_t last = causal ? p : kv_len - 1;
+            if (last > kv_len - 1)
+                last = kv_len - 1;
+            if (key_hi - 1 < last)
+                last = key_hi - 1;
+            int64_t first = key_lo > 0 ? key_lo : 0;
+            for (int h = 0; h < num_heads; h++) {
+                const uint16_t *qn = q_nope + (t * num_heads + h) * dc;
+                const uint16_t *qp = dp > 0 ? q_pe + (t * num_heads + h) * dp : NULL;
+                double *o = out + (t * num_heads + h) * dc;
+                for (int d = 0; d < dc; d++)
+                    o[d] = 0.0;
+                if (last < first) {
+                    lse[t * num_heads + h] = -INFINITY;
+                    continue;
+                }
+                double m = -INFINITY;
+                for (int64_t j = first; j <= last; j++) {
+                    int64_t page = kv_indices[kv_indptr[b] + j / page_size];
+                    int64_t slot = j % page_size;
+                    const uint16_t *c = ckv_cache + (page * page_size + slot) * dc;
+                    double dot = 0.0;
+                    for (int d = 0; d < dc; d++)
+                        dot += bf16_value(qn[d]) * bf16_value(c[d]);
+                    if (dp > 0) {
+                        const uint16_t *kp = kpe_cache + (page * page_size + slot) * dp;
+                        for (int d = 0; d < dp; d++)
+                            dot += bf16_value(qp[d]) * bf16_value(kp[d]);
+                    }
+                    scores[j - first] = sm_scale * dot;
+                    if (scores[j - first] > m)
+                        m = scores[j - first];
+                }
+                double denom = 0.0;
+                for (int64_t j = first; j <= last; j++) {
+                    scores[j - first] = exp(scores[j - first] - m);
+                    denom += scores[j - first];
+                }
+                for (int64_t j = first; j <= last; j++) {
+                    int64_t page = kv_indices[kv_indptr[b] + j / page_size];
+                    int64_t slot = j % page_size;
+                    const uint16_t *c = ckv_cache + (page * page_size + slot) * dc;
+                    double w = scores[j - first] / denom;
+                    for (int d = 0; d < dc; d++)
+                        o[d] += w * bf16_value(c[d]);
+                }
+                lse[t * num_heads + h] = m + log(denom);
+            }
+        }
+    }
+    free(scores);
+    return ORACLE_OK;
+}

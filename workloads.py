@@ -207,6 +207,89 @@ def _part_pages(call: Call):
     return [call.kv_indices[kvp[i]:kvp[i + 1]] for i in range(call.batch)]
 
 
+@dataclass
+class MLAStore:
+    """Latent rows of a set of sequences in one paged latent cache (multi-head
+    latent attention): ckv_cache [num_pages, page_size, dc] and kpe_cache
+    [num_pages, page_size, dp] bf16, q_nope [new, H, dc] / q_pe [new, H, dp]
+    per sequence.  Slots past a sequence's end hold NaN."""
+    seqs: list
+    num_heads: int
+    dc: int
+    dp: int
+    page_size: int
+    device: str
+    layout_seed: int = 7
+    ckv_cache: torch.Tensor = field(init=False)
+    kpe_cache: torch.Tensor = field(init=False)
+    q_nope: list = field(init=False)
+    q_pe: list = field(init=False)
+    pages: list = field(init=False)
+
+    def __post_init__(self):
+        P = self.page_size
+        counts = [-(-s.length // P) for s in self.seqs]
+        num_pages = max(sum(counts), 1)
+        perm = torch.randperm(num_pages, generator=_gen(self.layout_seed, "cpu"))
+        self.ckv_cache = torch.full((num_pages, P, self.dc), float("nan"), dtype=BF16,
+                                    device=self.device)
+        self.kpe_cache = torch.full((num_pages, P, self.dp), float("nan"), dtype=BF16,
+                                    device=self.device)
+        self.q_nope, self.q_pe, self.pages = [], [], []
+        start = 0
+        for s, c in zip(self.seqs, counts):
+            ids = perm[start:start + c].to(torch.int32)
+            start += c
+            self.pages.append(ids)
+            base = 4 * int(s.seed)
+            self.q_nope.append(draw_normal_bf16((s.new, self.num_heads, self.dc), base + 1,
+                                                self.device))
+            self.q_pe.append(draw_normal_bf16((s.new, self.num_heads, self.dp), base + 2,
+                                              self.device))
+            if c == 0:
+                continue
+            for cache, sub, width in ((self.ckv_cache, 3, self.dc), (self.kpe_cache, 0, self.dp)):
+                rows = draw_normal_bf16((s.length, width), base + sub, self.device)
+                padded = torch.full((c * P, width), float("nan"), dtype=BF16, device=self.device)
+                padded[: s.length] = rows
+                cache[ids.to(self.device).long()] = padded.view(c, P, width)
+
+
+@dataclass
+class MLACall:
+    store: MLAStore
+    q_nope: torch.Tensor
+    q_pe: torch.Tensor
+    qo_indptr: torch.Tensor  # int32, CPU
+    kv_indptr: torch.Tensor
+    kv_indices: torch.Tensor
+    kv_last_page_len: torch.Tensor
+    q_lens: list
+    kv_lens: list
+
+
+def mla_call(store: MLAStore, parts) -> MLACall:
+    """CSR description of an MLA call; parts are (sequence, q_start, q_end)."""
+    P = store.page_size
+    qn, qp, q_lens, kv_lens, idx, last, qo, kvp = [], [], [], [], [], [], [0], [0]
+    for (si, a, b) in parts:
+        s = store.seqs[si]
+        kv_len = s.prefix + b
+        n_pages = -(-kv_len // P)
+        qn.append(store.q_nope[si][a:b])
+        qp.append(store.q_pe[si][a:b])
+        q_lens.append(b - a)
+        kv_lens.append(kv_len)
+        idx.append(store.pages[si][:n_pages])
+        last.append(kv_len - (n_pages - 1) * P if n_pages > 0 else 0)
+        qo.append(qo[-1] + (b - a))
+        kvp.append(kvp[-1] + n_pages)
+    return MLACall(store, torch.cat(qn, 0).contiguous(), torch.cat(qp, 0).contiguous(),
+                   torch.tensor(qo, dtype=torch.int32), torch.tensor(kvp, dtype=torch.int32),
+                   torch.cat(idx).to(torch.int32).cpu(), torch.tensor(last, dtype=torch.int32),
+                   q_lens, kv_lens)
+
+
 def custom_mask(call: Call, seed: int, density: float = 0.7, causal_part: bool = False):
     """A seeded custom mask for a call: per request a [q_len, kv_len] boolean
     matrix (True = the token may see the key), i.i.d. Bernoulli(density), and
