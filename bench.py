@@ -437,6 +437,30 @@ def run_sweep(args):
          kv_bytes(c, 8, 256), cm, km)
     del st, c
     torch.cuda.empty_cache()
+    # multi-head latent attention decode: 16 heads over one 512 + 64 latent cache
+    ctx = wl.uniform_lengths(64, 1024, 32768, 4000)
+    mst = wl.MLAStore([wl.Sequence(7700 + i, c - 1, 1) for i, c in enumerate(ctx)], 16, 512, 64,
+                      1, dev, layout_seed=7997)
+    mc = wl.mla_call(mst, [(i, 0, 1) for i in range(len(mst.seqs))])
+    mdesc = bia.make_mla_desc(16, 1, 1.0 / 192 ** 0.5)
+    mws = torch.empty(bia.bia_mla_decode_workspace_size(mdesc, mc.kv_indptr,
+                                                        mc.kv_last_page_len),
+                      dtype=torch.uint8, device=dev)
+    mout = torch.empty((64, 16, 512), dtype=torch.bfloat16, device=dev)
+    margs = [mc.kv_indptr.to(dev), mc.kv_indices.to(dev), mc.kv_last_page_len.to(dev)]
+
+    def mla_f(evs):
+        if evs:
+            bia.bia_set_profile_events(*evs)
+        bia.bia_mla_decode_paged(mdesc, mc.q_nope, mc.q_pe, mst.ckv_cache, mst.kpe_cache, *margs,
+                                 mc.kv_indptr, mc.kv_last_page_len, mws, mout, stream=stream)
+        if evs:
+            bia.bia_set_profile_events(None, None)
+    cm, km = time_calls([mla_f])
+    emit("MLA decode B=64, 16 heads, latent 512+64 (ctx U[1024,32768], page 1)", "decode",
+         sum(mc.kv_lens) * (512 + 64) * 2, cm, km)
+    del mst, mc, mws, mout
+    torch.cuda.empty_cache()
     for B in (1, 8, 64, 256):
         st = wl.cfg4_decode(dev, B)
         c = wl.whole_prefill(st)

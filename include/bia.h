@@ -192,6 +192,45 @@ BIA_API int bia_decode_paged_noalloc(const bia_attn_desc *desc, const void *q, c
                              int32_t batch, int32_t split_size, void *out, float *lse,
                              void *stream);
 
+/* Multi-head latent attention: the latent (value) width and its rope width. */
+#define BIA_MLA_CKV_DIM 512
+#define BIA_MLA_KPE_DIM 64
+
+typedef struct bia_mla_desc {
+    int32_t num_heads; /* q heads; a multiple of 8 */
+    int32_t page_size; /* power of two, 1..256 */
+    float sm_scale;    /* <= 0: 1/sqrt(512 + 64) */
+} bia_mla_desc;
+
+/*
+ * Batch-invariant multi-head latent attention (MLA) decode over a paged latent
+ * cache: the paged MLA wrapper the pages name, which has no deterministic mode
+ * there ("sglang PR #43612", Summary), with the decode path's fixed split-KV
+ * tiles and ascending merge ("sglang PR #10417", Modifications).  Every q head
+ * attends to the one shared latent cache:
+ *   s_j = sm_scale * (<q_nope, ckv_j> + <q_pe, kpe_j>),
+ *   out = sum_j softmax(s)_j * ckv_j,  lse = natural-log LSE of s.
+ *   q_nope    [batch, num_heads, 512] bf16, q_pe [batch, num_heads, 64] bf16
+ *   ckv_cache [num_pages, page_size, 512] bf16, kpe_cache [num_pages, page_size, 64]
+ *   out       [batch, num_heads, 512] bf16, lse [batch, num_heads] fp32 or NULL
+ * The page table, split_size (0 = BIA_DECODE_SPLIT), workspace, ownership and
+ * error rules are those of bia_decode_paged; every request owns at least one
+ * key.  Outputs of a request never depend on the batch.
+ */
+BIA_API int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
+                         const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
+                         const int32_t *kv_indptr, const int32_t *kv_indices,
+                         const int32_t *kv_last_page_len, const int32_t *kv_indptr_host,
+                         const int32_t *kv_last_page_len_host, int32_t batch, int32_t split_size,
+                         void *workspace, size_t workspace_bytes, void *out, float *lse,
+                         void *stream);
+
+/* Workspace bytes bia_mla_decode_paged needs for this call (0 on invalid input). */
+BIA_API size_t bia_mla_decode_workspace_size(const bia_mla_desc *desc,
+                                     const int32_t *kv_indptr_host,
+                                     const int32_t *kv_last_page_len_host, int32_t batch,
+                                     int32_t split_size);
+
 /*
  * Fixed-order log-sum-exp merge of attention states (the merge the split-KV
  * partials of "sglang PR #10417", Modifications, need; the pages fix only

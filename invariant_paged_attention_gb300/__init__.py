@@ -33,7 +33,8 @@ EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged"
            "bia_decode_workspace_size", "bia_merge_states", "bia_q_tile_tokens",
            "bia_status_string", "bia_read_status", "bia_set_profile_events",
            "bia_launch_count", "bia_last_error", "bia_decode_paged_noalloc",
-           "bia_append_paged_kv", "bia_prefill_paged_mask")
+           "bia_append_paged_kv", "bia_prefill_paged_mask", "bia_mla_decode_paged",
+           "bia_mla_decode_workspace_size")
 
 
 class BiaError(RuntimeError):
@@ -52,6 +53,14 @@ class AttnDesc(ctypes.Structure):
 
 
 _lib = None
+
+
+class MlaDesc(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float)]
+
+
+MLA_CKV_DIM, MLA_KPE_DIM = 512, 64
 
 
 def load(path: str = LIB_PATH):
@@ -98,6 +107,12 @@ def load(path: str = LIB_PATH):
     lib.bia_prefill_paged_mask.argtypes = [dp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                            i32, i32, vp, sz, vp, vp, vp, sz, vp, vp, vp]
     lib.bia_prefill_paged_mask.restype = ctypes.c_int
+    mp = ctypes.POINTER(MlaDesc)
+    lib.bia_mla_decode_paged.argtypes = [mp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, i32, i32,
+                                         vp, sz, vp, vp, vp]
+    lib.bia_mla_decode_paged.restype = ctypes.c_int
+    lib.bia_mla_decode_workspace_size.argtypes = [mp, vp, vp, i32, i32]
+    lib.bia_mla_decode_workspace_size.restype = sz
     _lib = lib
     return lib
 
@@ -264,3 +279,28 @@ def bia_set_profile_events(begin=None, end=None):
 
 def bia_launch_count() -> int:
     return int(load().bia_launch_count())
+
+
+def make_mla_desc(num_heads, page_size, sm_scale=0.0) -> MlaDesc:
+    return MlaDesc(num_heads, page_size, float(sm_scale))
+
+
+def bia_mla_decode_workspace_size(desc, kv_indptr_host, kv_last_page_len_host,
+                                  split_size=0) -> int:
+    kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
+    return int(load().bia_mla_decode_workspace_size(ctypes.byref(desc), _ptr(kvp), _ptr(last),
+                                                    len(kvp) - 1, int(split_size)))
+
+
+def bia_mla_decode_paged(desc, q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices,
+                         kv_last_page_len, kv_indptr_host, kv_last_page_len_host, workspace,
+                         out, lse=None, split_size=0, stream=None):
+    """Multi-head latent attention decode (include/bia.h states the layouts)."""
+    kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
+    rc = load().bia_mla_decode_paged(
+        ctypes.byref(desc), _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+        ckv_cache.shape[0], _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len),
+        _ptr(kvp), _ptr(last), len(kvp) - 1, int(split_size), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_mla_decode_paged")

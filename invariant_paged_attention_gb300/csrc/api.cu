@@ -452,6 +452,126 @@ int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void
   return BIA_OK;
 }
 
+namespace {
+// Multi-head latent attention decode: validation and plan sizes as for the
+// GQA decode, with one shared 512 + 64 wide latent "kv head".
+int mla_plan(const bia_mla_desc *d, const int32_t *kvp_host, const int32_t *last_host,
+             int32_t batch, int32_t split, HostPlan *hp, bia_attn_desc *as_attn) {
+  if (!d || d->page_size <= 0) return BIA_ERR_INVALID_ARG;
+  if (d->num_heads <= 0 || d->num_heads % 8 != 0 || d->num_heads > 1024) return BIA_ERR_UNSUPPORTED;
+  if (!is_pow2(d->page_size) || d->page_size > 256) return BIA_ERR_UNSUPPORTED;
+  if (!std::isfinite(d->sm_scale)) return BIA_ERR_INVALID_ARG;
+  *as_attn = bia_attn_desc{d->num_heads, 1, BIA_MLA_CKV_DIM, d->page_size, d->sm_scale};
+  return host_plan(as_attn, nullptr, kvp_host, last_host, batch, 1, split, 1, 1, 1, hp);
+}
+} // namespace
+
+size_t bia_mla_decode_workspace_size(const bia_mla_desc *desc, const int32_t *kv_indptr_host,
+                                     const int32_t *kv_last_page_len_host, int32_t batch,
+                                     int32_t split_size) {
+  if (split_size == 0) split_size = BIA_DECODE_SPLIT;
+  HostPlan hp;
+  bia_attn_desc ad;
+  if (mla_plan(desc, kv_indptr_host, kv_last_page_len_host, batch, split_size, &hp, &ad) !=
+      BIA_OK)
+    return 0;
+  return bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows, desc->num_heads,
+                          BIA_MLA_CKV_DIM)
+      .total;
+}
+
+int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
+                         const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
+                         const int32_t *kv_indptr, const int32_t *kv_indices,
+                         const int32_t *kv_last_page_len, const int32_t *kv_indptr_host,
+                         const int32_t *kv_last_page_len_host, int32_t batch, int32_t split_size,
+                         void *workspace, size_t workspace_bytes, void *out, float *lse,
+                         void *stream) {
+  if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indptr || !kv_indices ||
+      !kv_last_page_len || !out || !workspace || num_pages <= 0)
+    return BIA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BIA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_nope) & 15u) || (reinterpret_cast<uintptr_t>(q_pe) & 15u) ||
+      (reinterpret_cast<uintptr_t>(ckv_cache) & 15u) ||
+      (reinterpret_cast<uintptr_t>(kpe_cache) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u))
+    return BIA_ERR_INVALID_ARG;
+  if (split_size == 0) split_size = BIA_DECODE_SPLIT;
+  HostPlan hp;
+  bia_attn_desc ad;
+  int rc = mla_plan(desc, kv_indptr_host, kv_last_page_len_host, batch, split_size, &hp, &ad);
+  if (rc != BIA_OK) return rc;
+  const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows,
+                                      desc->num_heads, BIA_MLA_CKV_DIM);
+  if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  PlanArgs pa{};
+  pa.qo_indptr = nullptr;
+  pa.kv_indptr = kv_indptr;
+  pa.kv_last_page_len = kv_last_page_len;
+  pa.batch = batch;
+  pa.page_size = desc->page_size;
+  pa.tile_tokens = 1;
+  pa.tiles_per_unit = 1;
+  pa.ctas = 1;
+  pa.causal = 1;
+  pa.split = split_size;
+  pa.n_groups_expected = hp.n_groups;
+  pa.n_units_expected = hp.n_units;
+  pa.part_rows_expected = hp.part_rows;
+  pa.status = reinterpret_cast<int32_t *>(ws + w.status);
+  pa.reqs = reinterpret_cast<bia::ReqInfo *>(ws + w.reqs);
+  pa.group_off = reinterpret_cast<int32_t *>(ws + w.group_off);
+  pa.group_cnt = reinterpret_cast<int32_t *>(ws + w.group_cnt);
+  pa.units = reinterpret_cast<bia::Unit *>(ws + w.units);
+  cudaError_t e = bia::launch_plan(pa, st);
+  if (e != cudaSuccess) return cuda_fail("plan kernel launch", e);
+  __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t *>(q_nope);
+  a.q_pe = static_cast<const uint16_t *>(q_pe);
+  a.k_cache = static_cast<const uint16_t *>(ckv_cache);
+  a.kpe_cache = static_cast<const uint16_t *>(kpe_cache);
+  a.kv_indices = kv_indices;
+  a.num_pages = num_pages;
+  a.Hq = desc->num_heads;
+  a.Hkv = 1;
+  a.D = BIA_MLA_CKV_DIM;
+  a.G = desc->num_heads;
+  a.page_shift = log2i(desc->page_size);
+  a.causal = 1;
+  a.split = split_size;
+  a.tile_tokens = 1;
+  const float sc = desc->sm_scale > 0.f
+                       ? desc->sm_scale
+                       : 1.0f / std::sqrt(static_cast<float>(BIA_MLA_CKV_DIM + BIA_MLA_KPE_DIM));
+  a.scale_log2 = sc * 1.4426950408889634f;
+  a.batch = batch;
+  a.n_units = hp.n_units;
+  a.reqs = pa.reqs;
+  a.units = pa.units;
+  a.part_o = reinterpret_cast<float *>(ws + w.part_o);
+  a.part_lse = reinterpret_cast<float *>(ws + w.part_lse);
+  a.total_rows = hp.total_q;
+  a.out = static_cast<uint16_t *>(out);
+  a.lse = lse;
+  a.status = pa.status;
+  const bool profile = g_attn_begin != nullptr && g_attn_end != nullptr;
+  if (profile && cudaEventRecord(g_attn_begin, st) != cudaSuccess) return BIA_ERR_CUDA;
+  e = bia::launch_mla_decode(a, st);
+  if (e != cudaSuccess) return cuda_fail("mla decode kernel launch", e);
+  __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  if (profile && cudaEventRecord(g_attn_end, st) != cudaSuccess) return BIA_ERR_CUDA;
+  if (hp.part_rows > 0) {
+    e = bia::launch_merge_partials(a, st);
+    if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
+    __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  }
+  return BIA_OK;
+}
+
 int32_t bia_q_tile_tokens(int32_t gqa_group) {
   if (gqa_group <= 0 || bia::kTileRows % gqa_group != 0) return 0;
   return bia::kTileRows / gqa_group;

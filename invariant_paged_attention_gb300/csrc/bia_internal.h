@@ -23,7 +23,9 @@ constexpr int kPrefillTilesPerUnit = 2; // q tiles sharing one K/V stream in a p
 inline int prefill_tiles_per_unit(int head_dim) {
   return head_dim == 256 ? 1 : kPrefillTilesPerUnit;
 }
-constexpr int kPrefillClusterCtas = 4;  // prefill CTAs of a cluster sharing each K/V gather
+constexpr int kPrefillClusterCtas = 4;
+constexpr int kMlaCkvDim = 512; // latent (value) width of multi-head latent attention
+constexpr int kMlaKpeDim = 64;  // its rope key width  // prefill CTAs of a cluster sharing each K/V gather
 
 // Per-request record written by the plan kernel.
 struct ReqInfo {
@@ -148,6 +150,9 @@ struct AttnArgs {
   // D] in 64-column boxes one row high; all SW128
   CUtensorMap tm_q, tm_k, tm_v;
   int32_t q_rows, kv_rows; // row extents of the maps (a row >= extent reads as zeros)
+  // multi-head latent attention (decode): q_pe [B, H, 64] and the rope rows
+  // of the latent cache [num_pages, P, 64]; q holds q_nope, k_cache the ckv rows
+  const uint16_t *q_pe, *kpe_cache;
   // optional custom mask (prefill): little-endian bit string of mask_words
   // 32-bit words; request b's [q_len, kv_len] bits start at bit mask_indptr[b]
   const uint32_t *mask;
@@ -171,6 +176,7 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_wide(const AttnArgs &a, cudaStream_t s); // head_dim 256
+cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_merge_states(const float *v, const float *s, const int32_t *num_states,
                                 int64_t n, int32_t S, int32_t H, int32_t D, uint16_t *out,

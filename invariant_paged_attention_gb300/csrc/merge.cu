@@ -147,8 +147,10 @@ cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t st) {
   const unsigned grid = static_cast<unsigned>(a.total_rows);
   if (a.D <= 128)
     merge_partials_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(a);
-  else // head_dim 256: eight floats per lane
+  else if (a.D <= 256) // head_dim 256: eight floats per lane
     merge_partials_kernel<8><<<grid, kMergeWarps * 32, 0, st>>>(a);
+  else // the 512-wide latent rows of multi-head latent attention
+    merge_partials_kernel<16><<<grid, kMergeWarps * 32, 0, st>>>(a);
   return cudaGetLastError();
 }
 
