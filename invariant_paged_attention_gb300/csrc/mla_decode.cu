@@ -13,9 +13,10 @@
 // stages with bulk copies.  A lane holds 16 of the 512 latent columns and 2 of
 // the 64 rope columns of its heads' queries (fp32, pre-scaled by
 // scale * log2 e) and of their outputs; a key's score is the butterfly sum of
-// the 32 lanes' partial dot products (the same bits on every lane), and each
-// head runs its online softmax over the keys in order, rescaled lazily when
-// the max grows by more than 2^8.
+// the 32 lanes' partial dot products (the same bits on every lane; four keys'
+// sums reduced together), and each head runs its online softmax over groups
+// of four keys in order, rescaled lazily when the group max exceeds the
+// running max by more than 2^8.
 #include "bia_internal.h"
 #include "ptx.cuh"
 
@@ -28,6 +29,7 @@ constexpr int kDp = kMlaKpeDim;  // 64
 constexpr int kMWarps = 8;       // consumer warps
 constexpr int kMThreads = (kMWarps + 1) * 32;
 constexpr int kMChunk = 8;       // keys per stage
+constexpr int kMGroup = 4;       // keys whose scores are reduced together
 constexpr int kMStages = 6;
 constexpr float kMLazy = 8.0f;   // log2 units
 
@@ -52,12 +54,6 @@ __device__ __forceinline__ uint32_t lds32m(uint32_t addr) {
   uint32_t r;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
   return r;
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
 }
 
 // HPW: heads per consumer warp (1 or 2); the CTA takes 8 * HPW heads.
@@ -174,37 +170,70 @@ __global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const AttnArgs
       break;
     }
     const int n_keys = min(kMChunk, key_end - (key_begin + i * kMChunk));
-    for (int kl = 0; kl < n_keys; ++kl) {
-      const uint4 c0 = lds128m(sCkv(st) + kl * L::kCkvRow + lane * 32);
-      const uint4 c1 = lds128m(sCkv(st) + kl * L::kCkvRow + lane * 32 + 16);
-      const uint32_t cp = lds32m(sKpe(st) + kl * L::kKpeRow + lane * 4);
-      const uint64_t c2[8] = {bf16x2_to_f32x2(c0.x), bf16x2_to_f32x2(c0.y),
-                              bf16x2_to_f32x2(c0.z), bf16x2_to_f32x2(c0.w),
-                              bf16x2_to_f32x2(c1.x), bf16x2_to_f32x2(c1.y),
-                              bf16x2_to_f32x2(c1.z), bf16x2_to_f32x2(c1.w)};
-      const uint64_t p2 = bf16x2_to_f32x2(cp);
+    // keys in groups of kMGroup: the group's scores are reduced together (their
+    // shuffle chains overlap) and its max drives one lazy-rescale decision;
+    // rows past the split's end are zero-filled and left out
+    for (int k0 = 0; k0 < n_keys; k0 += kMGroup) {
+      float sc[HPW][kMGroup];
+#pragma unroll
+      for (int q = 0; q < kMGroup; ++q) {
+        const uint32_t row = sCkv(st) + (k0 + q) * L::kCkvRow + lane * 32;
+        const uint4 c0 = lds128m(row);
+        const uint4 c1 = lds128m(row + 16);
+        const uint64_t p2 = bf16x2_to_f32x2(lds32m(sKpe(st) + (k0 + q) * L::kKpeRow + lane * 4));
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int k = 0; k < HPW; ++k) {
+          uint64_t acc = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ffma2(acc, qn[k][e], bf16x2_to_f32x2(cw[e]));
+          ffma2(acc, qp[k], p2);
+          float x, y;
+          f32x2_split(acc, x, y);
+          sc[k][q] = x + y;
+        }
+      }
+      // butterfly sums over the warp: the same bits on every lane
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int k = 0; k < HPW; ++k)
+#pragma unroll
+          for (int q = 0; q < kMGroup; ++q) sc[k][q] += __shfl_xor_sync(0xffffffffu, sc[k][q], off);
+      float pw[HPW][kMGroup];
 #pragma unroll
       for (int k = 0; k < HPW; ++k) {
-        uint64_t acc = 0;
+        float mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ffma2(acc, qn[k][e], c2[e]);
-        ffma2(acc, qp[k], p2);
-        float x, y;
-        f32x2_split(acc, x, y);
-        const float s = warp_sum(x + y); // log2 units; identical on every lane
-        if (s > m[k] + kMLazy || m[k] == -INFINITY) {
-          const float alpha = ex2(m[k] - s); // 0 when m == -inf
+        for (int q = 0; q < kMGroup; ++q)
+          if (k0 + q < n_keys) mx = fmaxf(mx, sc[k][q]);
+        if (mx > m[k] + kMLazy || m[k] == -INFINITY) {
+          const float alpha = ex2(m[k] - mx); // 0 when m == -inf
           l[k] *= alpha;
           const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
           for (int e = 0; e < 8; ++e) o2[k][e] = fmul2(o2[k][e], a2);
-          m[k] = s;
+          m[k] = mx;
         }
-        const float p = ex2(s - m[k]);
-        l[k] += p;
-        const uint64_t pp = f32x2(p, p);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ffma2(o2[k][e], pp, c2[e]);
+        for (int q = 0; q < kMGroup; ++q) {
+          pw[k][q] = k0 + q < n_keys ? ex2(sc[k][q] - m[k]) : 0.f;
+          l[k] += pw[k][q];
+        }
+      }
+      // P.V: the group's latent rows read again from shared memory
+#pragma unroll
+      for (int q = 0; q < kMGroup; ++q) {
+        const uint32_t row = sCkv(st) + (k0 + q) * L::kCkvRow + lane * 32;
+        const uint4 c0 = lds128m(row);
+        const uint4 c1 = lds128m(row + 16);
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int k = 0; k < HPW; ++k) {
+          const uint64_t pp = f32x2(pw[k][q], pw[k][q]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ffma2(o2[k][e], pp, bf16x2_to_f32x2(cw[e]));
+        }
       }
     }
     __syncwarp();
