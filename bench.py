@@ -660,11 +660,11 @@ def main():
                 "peak_source": f"bf16 dense burst, of {peak_kind}",
                 "algorithmic_flops_per_launch": flops, "kernel_ms": pk_avg * 1e3,
                 "traffic": traffic_from_profiles("prefill_kernel<128>", pre_src, flops)}
-    dec_roof = {"bound": "hbm", "kernel": "decode_kernel<128,4>", "achieved": dk_achieved,
+    dec_roof = {"bound": "hbm", "kernel": "decode_kernel<128,4,false>", "achieved": dk_achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dk_achieved / peaks["hbm_gbs"],
                 "peak_source": f"HBM copy, of {peak_kind}", "kv_bytes_per_launch": dbytes,
                 "kernel_ms": dk_avg * 1e3,
-                "traffic": traffic_from_profiles("decode_kernel<128,4>", dec_src, dbytes)
+                "traffic": traffic_from_profiles("decode_kernel<128,4,false>", dec_src, dbytes)
                 if decode else None}
 
     cpu = None

@@ -34,6 +34,7 @@ using bia::WsLayout;
 struct HostPlan {
   int64_t n_groups = 0;
   int64_t n_units = 0;
+  int64_t n_sunits = 0; // streamed single-token q tiles x their split tiles
   int64_t part_rows = 0;
   int64_t total_q = 0;
 };
@@ -62,9 +63,10 @@ int check_desc(const bia_attn_desc *d) {
 
 // Validates the host mirrors and computes the same plan sizes the device
 // planner will produce.  qo == nullptr: decode (one query per request).
+// stream: single-token tail tiles become streamed units (prefill).
 int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
               const int32_t *last, int32_t batch, int32_t causal, int32_t split, int tile_tokens,
-              int tiles_per_unit, int ctas, HostPlan *hp) {
+              int tiles_per_unit, int ctas, int stream, HostPlan *hp) {
   if (batch <= 0 || !kvp || !last) return BIA_ERR_INVALID_ARG;
   if (split <= 0 || split % bia::kKvBlock != 0) return BIA_ERR_UNSUPPORTED;
   if (qo && qo[0] != 0) return BIA_ERR_INVALID_ARG;
@@ -79,16 +81,19 @@ int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
     if (kv_len > INT32_MAX / 2) return BIA_ERR_UNSUPPORTED;
     if (causal && q_len > kv_len) return BIA_ERR_INVALID_ARG;
     if (!qo && kv_len == 0) return BIA_ERR_INVALID_ARG;
-    int32_t nsp = 1;
-    const int64_t tiles = (q_len + tile_tokens - 1) / tile_tokens;
+    int32_t nsp = 1, ns = 0;
+    const int64_t tiles = bia::tensor_tiles(static_cast<int32_t>(q_len), tile_tokens, stream);
     const int64_t gt = bia::group_tiles(tiles_per_unit, ctas);
     p.n_groups += (tiles + gt - 1) / gt;
     p.n_units += bia::request_units(static_cast<int32_t>(q_len), static_cast<int32_t>(kv_len),
-                                    tile_tokens, tiles_per_unit, ctas, causal, split, &nsp);
+                                    tile_tokens, tiles_per_unit, ctas, causal, split, stream,
+                                    &nsp, &ns);
+    p.n_sunits += ns;
     if (nsp > 1) p.part_rows += q_len * nsp;
     p.total_q += q_len;
   }
   if (p.n_units > INT32_MAX) return BIA_ERR_UNSUPPORTED; // grid.x limit is 2^31-1
+  if (p.n_sunits * d->num_kv_heads > INT32_MAX) return BIA_ERR_UNSUPPORTED;
   *hp = p;
   return BIA_OK;
 }
@@ -197,17 +202,18 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
   const int tiles_per_unit = decode ? 1 : bia::prefill_tiles_per_unit(desc->head_dim);
   const int ctas = decode ? 1 : bia::kPrefillClusterCtas;
+  const int stream_tail = decode ? 0 : 1;
   if (decode) causal = 1;
   HostPlan hp;
   rc = host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal, split,
-                 tile_tokens, tiles_per_unit, ctas, &hp);
+                 tile_tokens, tiles_per_unit, ctas, stream_tail, &hp);
   if (rc != BIA_OK) return rc;
   if (mask) {
     rc = check_mask(*mask, qo_host, kvp_host, last_host, batch, desc->page_size);
     if (rc != BIA_OK) return rc;
   }
-  const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows,
-                                      desc->num_qo_heads, desc->head_dim);
+  const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.n_sunits,
+                                      hp.part_rows, desc->num_qo_heads, desc->head_dim);
   if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
   if (hp.total_q == 0) return BIA_OK;
 
@@ -229,14 +235,17 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   pa.ctas = ctas;
   pa.causal = causal;
   pa.split = split;
+  pa.stream = stream_tail;
   pa.n_groups_expected = hp.n_groups;
   pa.n_units_expected = hp.n_units;
+  pa.n_sunits_expected = hp.n_sunits;
   pa.part_rows_expected = hp.part_rows;
   pa.status = reinterpret_cast<int32_t *>(ws + w.status);
   pa.reqs = reinterpret_cast<bia::ReqInfo *>(ws + w.reqs);
   pa.group_off = reinterpret_cast<int32_t *>(ws + w.group_off);
   pa.group_cnt = reinterpret_cast<int32_t *>(ws + w.group_cnt);
   pa.units = reinterpret_cast<bia::Unit *>(ws + w.units);
+  pa.sunits = reinterpret_cast<bia::Unit *>(ws + w.sunits);
   cudaError_t pe = bia::launch_plan(pa, st);
   if (pe != cudaSuccess) return cuda_fail("plan kernel launch", pe);
   __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
@@ -289,6 +298,14 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
                                           : bia::launch_prefill(a, st);
   if (e != cudaSuccess) return cuda_fail(decode ? "decode kernel launch" : "prefill kernel launch", e);
   if (hp.n_units > 0) __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  if (hp.n_sunits > 0) { // single-token q tiles of a prefill call, streamed
+    AttnArgs sa = a;
+    sa.units = pa.sunits;
+    sa.n_units = hp.n_sunits;
+    e = bia::launch_decode(sa, st);
+    if (e != cudaSuccess) return cuda_fail("streamed-tile kernel launch", e);
+    __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  }
   if (profile && cudaEventRecord(g_attn_end, st) != cudaSuccess) return BIA_ERR_CUDA;
   if (hp.part_rows > 0) {
     e = bia::launch_merge_partials(a, st);
@@ -310,10 +327,10 @@ size_t workspace_size(bool decode, const bia_attn_desc *desc, const int32_t *qo_
   const int ctas = decode ? 1 : bia::kPrefillClusterCtas;
   HostPlan hp;
   if (host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, decode ? 1 : causal,
-                split, tile_tokens, tiles_per_unit, ctas, &hp) != BIA_OK)
+                split, tile_tokens, tiles_per_unit, ctas, decode ? 0 : 1, &hp) != BIA_OK)
     return 0;
-  return bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows, desc->num_qo_heads,
-                          desc->head_dim)
+  return bia::make_layout(batch, hp.n_groups, hp.n_units, hp.n_sunits, hp.part_rows,
+                          desc->num_qo_heads, desc->head_dim)
       .total;
 }
 
@@ -462,7 +479,7 @@ int mla_plan(const bia_mla_desc *d, const int32_t *kvp_host, const int32_t *last
   if (!is_pow2(d->page_size) || d->page_size > 256) return BIA_ERR_UNSUPPORTED;
   if (!std::isfinite(d->sm_scale)) return BIA_ERR_INVALID_ARG;
   *as_attn = bia_attn_desc{d->num_heads, 1, BIA_MLA_CKV_DIM, d->page_size, d->sm_scale};
-  return host_plan(as_attn, nullptr, kvp_host, last_host, batch, 1, split, 1, 1, 1, hp);
+  return host_plan(as_attn, nullptr, kvp_host, last_host, batch, 1, split, 1, 1, 1, 0, hp);
 }
 } // namespace
 
@@ -475,7 +492,7 @@ size_t bia_mla_decode_workspace_size(const bia_mla_desc *desc, const int32_t *kv
   if (mla_plan(desc, kv_indptr_host, kv_last_page_len_host, batch, split_size, &hp, &ad) !=
       BIA_OK)
     return 0;
-  return bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows, desc->num_heads,
+  return bia::make_layout(batch, hp.n_groups, hp.n_units, 0, hp.part_rows, desc->num_heads,
                           BIA_MLA_CKV_DIM)
       .total;
 }
@@ -500,7 +517,7 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
   bia_attn_desc ad;
   int rc = mla_plan(desc, kv_indptr_host, kv_last_page_len_host, batch, split_size, &hp, &ad);
   if (rc != BIA_OK) return rc;
-  const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.part_rows,
+  const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, 0, hp.part_rows,
                                       desc->num_heads, BIA_MLA_CKV_DIM);
   if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t *ws = static_cast<uint8_t *>(workspace);

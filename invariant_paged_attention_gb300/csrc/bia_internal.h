@@ -23,9 +23,9 @@ constexpr int kPrefillTilesPerUnit = 2; // q tiles sharing one K/V stream in a p
 inline int prefill_tiles_per_unit(int head_dim) {
   return head_dim == 256 ? 1 : kPrefillTilesPerUnit;
 }
-constexpr int kPrefillClusterCtas = 4;
+constexpr int kPrefillClusterCtas = 4; // prefill CTAs of a cluster sharing each K/V gather
 constexpr int kMlaCkvDim = 512; // latent (value) width of multi-head latent attention
-constexpr int kMlaKpeDim = 64;  // its rope key width  // prefill CTAs of a cluster sharing each K/V gather
+constexpr int kMlaKpeDim = 64;  // its rope key width
 
 // Per-request record written by the plan kernel.
 struct ReqInfo {
@@ -40,7 +40,9 @@ struct ReqInfo {
 static_assert(sizeof(ReqInfo) == 32, "ReqInfo layout");
 
 // One unit of work for one kv head (grid.y): q tiles tile .. tile+ntiles-1 of
-// request b against split-KV tile `split`.
+// request b against split-KV tile `split`.  A streamed unit (one query token
+// against one split tile, run by the decode kernel) holds the token's index
+// within its request in `tile` and 1 in `ntiles`.
 struct Unit {
   int32_t b, tile, split, ntiles;
 };
@@ -52,6 +54,7 @@ struct WsLayout {
   size_t group_off = 0; // int32[batch + 1]: first q-tile group of each request
   size_t group_cnt = 0; // int32[n_groups]: first unit of each group
   size_t units = 0;    // Unit[n_units]
+  size_t sunits = 0;   // Unit[n_sunits]: streamed single-token q tiles
   size_t part_o = 0;   // float[part_rows * Hq * D]
   size_t part_lse = 0; // float[part_rows * Hq]
   size_t total = 0;
@@ -75,42 +78,69 @@ __host__ __device__ inline int32_t tile_splits(int32_t q_len, int32_t kv_len, in
   return last < 0 ? 1 : last / split + 1;
 }
 
-// Units of one request: its q tiles grouped ctas * tiles_per_unit at a time,
-// each group crossed with the split tiles its last (widest) q tile touches;
-// a group's units for one split are `ctas` consecutive units (one per CTA of
-// a cluster, tiles_per_unit tiles each; the last ones may hold no tile).
+// A prefill request whose last q tile holds a single token (a one-token
+// extend, or the one-token tail of a longer chunk) has that tile streamed by
+// the decode kernel, one query row per CTA, instead of filling G of the 128
+// rows of a tensor-core tile.  The choice is a function of the tile alone (its
+// token count), and every q-tile-aligned chunking of a request cuts the same
+// tiles, so it holds the same way in any batch and any aligned chunking.
+__host__ __device__ inline int32_t streamed_tail(int32_t q_len, int32_t tile_tokens,
+                                                 int32_t stream) {
+  return stream && tile_tokens > 1 && q_len % tile_tokens == 1 ? 1 : 0;
+}
+// q tiles of a request that run on the tensor-core prefill kernel.
+__host__ __device__ inline int32_t tensor_tiles(int32_t q_len, int32_t tile_tokens,
+                                                int32_t stream) {
+  return (q_len + tile_tokens - 1) / tile_tokens - streamed_tail(q_len, tile_tokens, stream);
+}
+
+// Units of one request: its tensor q tiles grouped ctas * tiles_per_unit at a
+// time, each group crossed with the split tiles its last (widest) q tile
+// touches; a group's units for one split are `ctas` consecutive units (one per
+// CTA of a cluster, tiles_per_unit tiles each; the last ones may hold no
+// tile).  A streamed tail adds one streamed unit per split tile it touches
+// (*stream_units).
 __host__ __device__ inline int32_t group_tiles(int32_t tiles_per_unit, int32_t ctas) {
   return tiles_per_unit * ctas;
 }
 __host__ __device__ inline int64_t request_units(int32_t q_len, int32_t kv_len,
                                                  int32_t tile_tokens, int32_t tiles_per_unit,
                                                  int32_t ctas, int32_t causal, int32_t split,
-                                                 int32_t *max_splits) {
+                                                 int32_t stream, int32_t *max_splits,
+                                                 int32_t *stream_units) {
   const int32_t tiles = (q_len + tile_tokens - 1) / tile_tokens;
+  const int32_t tt = tensor_tiles(q_len, tile_tokens, stream);
   const int32_t gt = group_tiles(tiles_per_unit, ctas);
   int64_t units = 0;
   int32_t nsp = 1;
-  for (int32_t t0 = 0; t0 < tiles; t0 += gt) {
-    const int32_t last = min(t0 + gt, tiles) - 1;
+  for (int32_t t0 = 0; t0 < tt; t0 += gt) {
+    const int32_t last = min(t0 + gt, tt) - 1;
     const int32_t n = tile_splits(q_len, kv_len, last, tile_tokens, causal, split);
     units += static_cast<int64_t>(n) * ctas;
     if (n > nsp) nsp = n;
   }
+  int32_t ns = 0;
+  if (tt < tiles) {
+    ns = tile_splits(q_len, kv_len, tiles - 1, tile_tokens, causal, split);
+    if (ns > nsp) nsp = ns;
+  }
   if (max_splits) *max_splits = nsp;
+  if (stream_units) *stream_units = ns;
   return units;
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout make_layout(int batch, int64_t n_groups, int64_t n_units, int64_t part_rows,
-                            int Hq, int D) {
+inline WsLayout make_layout(int batch, int64_t n_groups, int64_t n_units, int64_t n_sunits,
+                            int64_t part_rows, int Hq, int D) {
   WsLayout w;
   w.status = 0;
   w.reqs = 256;
   w.group_off = align_up(w.reqs + sizeof(ReqInfo) * (size_t)batch, 256);
   w.group_cnt = align_up(w.group_off + sizeof(int32_t) * ((size_t)batch + 1), 256);
   w.units = align_up(w.group_cnt + sizeof(int32_t) * (size_t)n_groups, 256);
-  w.part_o = align_up(w.units + sizeof(Unit) * (size_t)n_units, 256);
+  w.sunits = align_up(w.units + sizeof(Unit) * (size_t)n_units, 256);
+  w.part_o = align_up(w.sunits + sizeof(Unit) * (size_t)n_sunits, 256);
   w.part_lse = align_up(w.part_o + sizeof(float) * (size_t)part_rows * Hq * D, 256);
   w.total = align_up(w.part_lse + sizeof(float) * (size_t)part_rows * Hq, 256);
   return w;
@@ -121,11 +151,12 @@ struct PlanArgs {
   const int32_t *kv_indptr;
   const int32_t *kv_last_page_len;
   int32_t batch, page_size, tile_tokens, tiles_per_unit, ctas, causal, split;
-  int64_t n_groups_expected, n_units_expected, part_rows_expected;
+  int32_t stream; // 1: single-token tail tiles become streamed units (prefill)
+  int64_t n_groups_expected, n_units_expected, n_sunits_expected, part_rows_expected;
   int32_t *status;
   ReqInfo *reqs;
   int32_t *group_off, *group_cnt;
-  Unit *units;
+  Unit *units, *sunits;
 };
 
 // Geometry of a call shared by the attention kernels.

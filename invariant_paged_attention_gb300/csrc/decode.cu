@@ -15,6 +15,13 @@
 // by more than 2^8; lane groups and then warps are combined in a fixed order,
 // so a request's partial and output have the same bits in any batch.
 //
+// The same kernel streams the single-token q tiles of a prefill call (a
+// one-token extend, or a request's one-token tail tile) with the prefill
+// split size: a unit then names its query token's index within the request,
+// the keys it sees end at its causal position, and with a custom mask a key
+// also needs its mask bit (a masked key is skipped exactly like a key past
+// the end, so a mask that hides nothing visible gives the unmasked bits).
+//
 // The fixed split of 2048 keys per tile and the merge of the tiles' partials
 // follow "sglang PR #10417 [POC] Support deterministic inference",
 // Modifications (split-KV fixed to 2048 for decode).
@@ -98,7 +105,7 @@ __device__ __forceinline__ float reduce_scatter4(const float (&s)[4]) {
   return c;
 }
 
-template <int D, int G>
+template <int D, int G, bool MASK>
 __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     decode_kernel(const AttnArgs a) {
   using L = DecSmem<D>;
@@ -125,8 +132,14 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
   const ReqInfo r = a.reqs[u.b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPK, sub = lane % LPK;
+  // the query: token t of the request (0 for decode); it sees keys < q_end
+  const int32_t t = u.tile;
+  const int32_t q_end = a.causal ? r.kv_len - r.q_len + t + 1 : r.kv_len;
+  const int64_t q_row = static_cast<int64_t>(r.q_start) + t;
   const int32_t key_begin = u.split * a.split;
-  const int32_t key_end = min(key_begin + a.split, r.kv_len);
+  const int32_t key_end = min(key_begin + a.split, q_end);
+  // custom mask: bit (t, key) of the request's [q_len, kv_len] mask
+  const int64_t mask_row = MASK ? a.mask_indptr[u.b] + static_cast<int64_t>(t) * r.kv_len : 0;
   const int n_chunks = (key_end - key_begin + kChunk - 1) / kChunk;
   const int my_chunks = warp < n_chunks ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
 
@@ -192,7 +205,7 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const uint4 w = sub * 8 < Dr ? *reinterpret_cast<const uint4 *>(
-        a.q + (static_cast<int64_t>(r.q_start) * a.Hq + kvh * G + g) * Dr + sub * 8)
+        a.q + (q_row * a.Hq + kvh * G + g) * Dr + sub * 8)
                                  : make_uint4(0u, 0u, 0u, 0u);
     const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2);
     q2[g][0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
@@ -235,7 +248,11 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
         f32x2_split(acc, x, y);
         sc[g] = x + y;
       }
-      const bool valid = key0 + kl < key_end; // past the split's last key: no weight
+      bool valid = key0 + kl < key_end; // past the split's last key: no weight
+      if constexpr (MASK) {
+        const int64_t bit = mask_row + key0 + kl;
+        valid = valid && ((__ldg(a.mask + (bit >> 5)) >> (bit & 31)) & 1u);
+      }
       const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
                               bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
       if constexpr (kOwnHead) {
@@ -348,7 +365,7 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
   }
   __syncthreads();
 
-  const bool single = (r.kv_len - 1) / a.split == 0; // one split: the final row
+  const bool single = (q_end - 1) / a.split == 0; // one split: the final row
   for (int e = threadIdx.x; e < G * D; e += kThreadsDec) {
     const int g = e / D, d = e % D;
     if (d >= Dr) continue;
@@ -368,32 +385,37 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
     const bool empty_row = !(Ls > 0.f);
     const float val = empty_row ? 0.f : __fdiv_rn(O, Ls);
     const float lse = empty_row ? -INFINITY : __fmul_rn(__fadd_rn(M, lg2(Ls)), kLn2);
-    const int64_t row = static_cast<int64_t>(r.q_start) * a.Hq + h;
+    const int64_t row = q_row * a.Hq + h;
     if (single) {
       a.out[row * Dr + d] = to_bf16(val);
       if (a.lse && d == 0) a.lse[row] = lse;
     } else {
-      const int64_t prow = (r.rowbase + u.split) * a.Hq + h;
+      const int64_t prow = (r.rowbase + static_cast<int64_t>(t) * r.nsp + u.split) * a.Hq + h;
       a.part_o[prow * Dr + d] = val;
       if (d == 0) a.part_lse[prow] = lse;
     }
   }
 }
 
-template <int D, int G>
-cudaError_t launch_decode_dg(const AttnArgs &a, cudaStream_t s) {
+template <int D, int G, bool MASK>
+cudaError_t launch_decode_dgm(const AttnArgs &a, cudaStream_t s) {
   using L = DecSmem<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, MASK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int64_t blocks = a.n_units * a.Hkv;
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
-  decode_kernel<D, G><<<static_cast<unsigned>(blocks), kThreadsDec, L::kAlloc, s>>>(a);
+  decode_kernel<D, G, MASK><<<static_cast<unsigned>(blocks), kThreadsDec, L::kAlloc, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_decode_dg(const AttnArgs &a, cudaStream_t s) {
+  return a.mask ? launch_decode_dgm<D, G, true>(a, s) : launch_decode_dgm<D, G, false>(a, s);
 }
 
 template <int D>

@@ -4,7 +4,9 @@
 // the status word.
 //
 //   A. per request: lengths, q-tile groups, split tiles of the widest tile,
-//      partial rows; block scans give group offsets and partial-row bases
+//      partial rows, streamed units of a single-token tail tile; block scans
+//      give group offsets, partial-row bases and streamed-unit offsets, and
+//      the streamed units are written here
 //   B. per group (all threads): its split count
 //   C. block scan of the split counts: each group's first unit
 //   D. per group: its units (the request's last groups first: they carry the
@@ -75,21 +77,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   // ---- A: per request
   const int per = (a.batch + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
-  int64_t my_groups = 0, my_rows = 0;
+  int64_t my_groups = 0, my_rows = 0, my_sunits = 0;
   for (int b = lo; b < hi; ++b) {
     int32_t q_start, q_len, kv_len;
     request_geometry(a, b, q_start, q_len, kv_len);
     const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
     const int32_t nsp = tiles > 0 ? tile_splits(q_len, kv_len, tiles - 1, a.tile_tokens,
                                                 a.causal, a.split) : 1;
-    my_groups += (tiles + gt - 1) / gt;
+    my_groups += (tensor_tiles(q_len, a.tile_tokens, a.stream) + gt - 1) / gt;
     if (nsp > 1) my_rows += static_cast<int64_t>(q_len) * nsp;
+    if (streamed_tail(q_len, a.tile_tokens, a.stream)) my_sunits += nsp;
   }
-  int64_t total_groups, total_rows;
+  int64_t total_groups, total_rows, total_sunits;
   int64_t group = block_exclusive_scan<int64_t>(my_groups, s_scan, &total_groups);
   int64_t row = block_exclusive_scan<int64_t>(my_rows, s_scan, &total_rows);
+  int64_t sunit = block_exclusive_scan<int64_t>(my_sunits, s_scan, &total_sunits);
+  // every thread sees the same totals: the streamed units below are written
+  // only when they fit the host-sized list
+  const bool sizes_ok = total_groups == a.n_groups_expected &&
+                        total_rows == a.part_rows_expected &&
+                        total_sunits == a.n_sunits_expected;
   if (tid == 0) {
-    s_ok = total_groups == a.n_groups_expected && total_rows == a.part_rows_expected;
+    s_ok = sizes_ok;
     if (s_ok) a.group_off[a.batch] = static_cast<int32_t>(total_groups);
   }
   for (int b = lo; b < hi; ++b) {
@@ -98,6 +107,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
     const int32_t nsp = tiles > 0 ? tile_splits(q_len, kv_len, tiles - 1, a.tile_tokens,
                                                 a.causal, a.split) : 1;
+    if (streamed_tail(q_len, a.tile_tokens, a.stream)) {
+      // the tail tile is the request's widest: its split count is nsp
+      for (int32_t sp = 0; sp < nsp; ++sp)
+        if (sizes_ok) a.sunits[sunit + sp] = Unit{b, q_len - 1, sp, 1};
+      sunit += nsp;
+    }
     const int64_t rows = nsp > 1 ? static_cast<int64_t>(q_len) * nsp : 0;
     ReqInfo r;
     r.q_start = q_start;
@@ -109,7 +124,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     r.pad = 0;
     a.reqs[b] = r;
     a.group_off[b] = static_cast<int32_t>(group);
-    group += (tiles + gt - 1) / gt;
+    group += (tensor_tiles(q_len, a.tile_tokens, a.stream) + gt - 1) / gt;
     row += rows;
   }
   __syncthreads();
@@ -120,7 +135,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     for (int32_t g = tid; g < n_groups; g += kPlanThreads) {
       const int b = find_group_owner(a.group_off, a.batch, g);
       const ReqInfo r = a.reqs[b];
-      const int32_t tiles = (r.q_len + a.tile_tokens - 1) / a.tile_tokens;
+      const int32_t tiles = tensor_tiles(r.q_len, a.tile_tokens, a.stream);
       const int32_t groups = (tiles + gt - 1) / gt;
       const int32_t gi = groups - 1 - (g - a.group_off[b]);
       const int32_t t0 = gi * gt;
@@ -147,6 +162,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (tid == 0) atomicOr(a.status, kStatusPlanMismatch);
     for (int64_t i = tid; i < a.n_units_expected; i += kPlanThreads)
       a.units[i] = Unit{-1, 0, 0, 0};
+    for (int64_t i = tid; i < a.n_sunits_expected; i += kPlanThreads)
+      a.sunits[i] = Unit{-1, 0, 0, 0};
     return;
   }
 
@@ -154,7 +171,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   for (int32_t g = tid; g < n_groups; g += kPlanThreads) {
     const int b = find_group_owner(a.group_off, a.batch, g);
     const ReqInfo r = a.reqs[b];
-    const int32_t tiles = (r.q_len + a.tile_tokens - 1) / a.tile_tokens;
+    const int32_t tiles = tensor_tiles(r.q_len, a.tile_tokens, a.stream);
     const int32_t groups = (tiles + gt - 1) / gt;
     const int32_t gi = groups - 1 - (g - a.group_off[b]);
     const int32_t t0 = gi * gt;
