@@ -215,7 +215,8 @@ typedef struct bia_mla_desc {
  *   out       [batch, num_heads, 512] bf16, lse [batch, num_heads] fp32 or NULL
  * The page table, split_size (0 = BIA_DECODE_SPLIT), workspace, ownership and
  * error rules are those of bia_decode_paged; every request owns at least one
- * key.  Outputs of a request never depend on the batch.
+ * key.  batch * num_heads and num_pages * page_size must stay below 2^31
+ * (else BIA_ERR_UNSUPPORTED).  Outputs of a request never depend on the batch.
  */
 BIA_API int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
                          const void *ckv_cache, const void *kpe_cache, int64_t num_pages,

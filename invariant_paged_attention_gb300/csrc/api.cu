@@ -131,6 +131,22 @@ int encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int head_d
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
+// A 2-D map over `rows` rows of `cols` bf16 (row pitch cols*2 bytes) in boxes
+// of 64 columns x box_rows rows, 128-byte swizzle; rows past the end read as
+// zeros.
+int encode_2d_map(CUtensorMap *map, const void *base, int64_t rows, int cols, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return -1;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return static_cast<int>(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
 // The q tiles of a prefill call as a 3-D map [total_q][Hq][head_dim]; a box
 // of 64 columns x G heads x T tokens is one 64-column half of a 128-row q
 // tile (rows = token-major (token, head) pairs, 128-byte swizzle); tokens past
@@ -575,6 +591,18 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
   a.out = static_cast<uint16_t *>(out);
   a.lse = lse;
   a.status = pa.status;
+  // tensor maps: the heads' q rows in 16-row boxes, the latent rows one row
+  // per box (gathered)
+  const int64_t q_rows = static_cast<int64_t>(batch) * desc->num_heads;
+  const int64_t kv_rows = num_pages * desc->page_size;
+  if (q_rows >= INT32_MAX || kv_rows >= INT32_MAX) return BIA_ERR_UNSUPPORTED;
+  a.q_rows = static_cast<int32_t>(q_rows);
+  a.kv_rows = static_cast<int32_t>(kv_rows);
+  int ce = encode_2d_map(&a.tm_q, q_nope, q_rows, BIA_MLA_CKV_DIM, bia::kMlaHeadGroup);
+  if (ce == 0) ce = encode_2d_map(&a.tm_qpe, q_pe, q_rows, BIA_MLA_KPE_DIM, bia::kMlaHeadGroup);
+  if (ce == 0) ce = encode_2d_map(&a.tm_k, ckv_cache, kv_rows, BIA_MLA_CKV_DIM, 1);
+  if (ce == 0) ce = encode_2d_map(&a.tm_kpe, kpe_cache, kv_rows, BIA_MLA_KPE_DIM, 1);
+  if (ce != 0) return fail(BIA_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable", ce);
   const bool profile = g_attn_begin != nullptr && g_attn_end != nullptr;
   if (profile && cudaEventRecord(g_attn_begin, st) != cudaSuccess) return BIA_ERR_CUDA;
   e = bia::launch_mla_decode(a, st);

@@ -181,6 +181,11 @@ struct AttnArgs {
   // D] in 64-column boxes one row high; all SW128
   CUtensorMap tm_q, tm_k, tm_v;
   int32_t q_rows, kv_rows; // row extents of the maps (a row >= extent reads as zeros)
+  // multi-head latent attention on the tensor cores: q_pe rows [B*H, 64] in
+  // 64 x 16-row boxes (tm_q then holds q_nope [B*H, 512] in the same boxes,
+  // tm_k the ckv rows [num_pages*P, 512] in 64 x 1 boxes) and the kpe rows
+  // [num_pages*P, 64] in 64 x 1 boxes
+  CUtensorMap tm_qpe, tm_kpe;
   // multi-head latent attention (decode): q_pe [B, H, 64] and the rope rows
   // of the latent cache [num_pages, P, 64]; q holds q_nope, k_cache the ckv rows
   const uint16_t *q_pe, *kpe_cache;
@@ -208,6 +213,7 @@ cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_wide(const AttnArgs &a, cudaStream_t s); // head_dim 256
 cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s);
+constexpr int kMlaHeadGroup = 16; // q heads per CTA of the MLA decode kernel
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_merge_states(const float *v, const float *s, const int32_t *num_states,
                                 int64_t n, int32_t S, int32_t H, int32_t D, uint16_t *out,

@@ -1,22 +1,59 @@
 // Batch-invariant multi-head latent attention (MLA) decode over a paged latent
-// cache.  The pages' serving stack runs Kimi-Linear's MLA through a paged MLA
-// wrapper that has no deterministic mode ("sglang PR #43612", Summary); this
-// is the same computation with the decode path's invariance: fixed split-KV
-// tiles of split_size keys anchored at key 0 ("sglang PR #10417 [POC] Support
-// deterministic inference", Modifications) folded in ascending order.
+// cache, on the tensor cores (tcgen05 + TMEM).  The pages' serving stack runs
+// Kimi-Linear's MLA through a paged MLA wrapper that has no deterministic mode
+// ("sglang PR #43612", Summary); this is the same computation with the decode
+// path's invariance: fixed split-KV tiles of split_size keys anchored at key 0
+// ("sglang PR #10417 [POC] Support deterministic inference", Modifications),
+// their partials folded in ascending order by the merge kernel.
 //
 // Every q head attends to the shared latent rows: s = scale * (<q_nope, ckv>
 // + <q_pe, kpe>), out = softmax(s) . ckv (the 512-wide latent row is also the
-// value).  One CTA per (request, split tile, group of 8 or 16 heads): warps
-// 0-7 each own 1 or 2 heads for all the split's keys, warp 8 streams the
-// latent rows (ckv 1 KB + kpe 128 B per key) into a shared ring of 8-key
-// stages with bulk copies.  A lane holds 16 of the 512 latent columns and 2 of
-// the 64 rope columns of its heads' queries (fp32, pre-scaled by
-// scale * log2 e) and of their outputs; a key's score is the butterfly sum of
-// the 32 lanes' partial dot products (the same bits on every lane; four keys'
-// sums reduced together), and each head runs its online softmax over groups
-// of four keys in order, rescaled lazily when the group max exceeds the
-// running max by more than 2^8.
+// value).  The MMAs take the keys as M and the heads as N: a decode query has
+// 16 to 128 heads, far fewer than the 128 rows of an M=128 tile, while a
+// 128-key block fills M exactly.
+//
+// One CTA per (request, split tile, group of 16 heads); keys in 128-key
+// blocks.  Per block:
+//   S^T = C Q^T     M=128 keys, N=16 heads, K=512+64: A = the latent rows
+//                   (K-major, 64-column SW128 pieces), B = the 16 heads'
+//                   q_nope / q_pe (K-major), fp32 accumulator in TMEM
+//   softmax         thread t = key t of the block (TMEM lane t) reads its 16
+//                   heads' scores; per-head block max = redux over the warp,
+//                   then over the 4 warps through shared memory (the same
+//                   value on every thread); lazy online softmax (the running
+//                   max moves only when the block max exceeds it by more than
+//                   2^8; O is then rescaled in TMEM); P = 2^(s - m) as bf16
+//                   into shared memory, row t = key t (MN-major operand)
+//   O^T += C^T P^T  four accumulators of M=128 latent columns, N=16 heads,
+//                   K=128 keys: A = the same latent pieces read MN-major
+//                   (two 64-column pieces side by side), B = P
+// Each thread keeps its own keys' partial row sums per head; the epilogue
+// sums them (warp butterfly, then the 4 warps in order) and writes
+// o = O^T / l and lse (bf16 rows for a request with one split, else fp32
+// partials).
+//
+// Warp roles (9 warps): 0-3 softmax + epilogue, 4 owns TMEM and issues every
+// MMA from one thread, 5-8 copy: one thread loads the 16 heads' q (2-D TMA
+// boxes), and the 128 threads copy the paged latent rows with 16-byte cp.async
+// straight into the swizzled operand layout (keys past the split or on a bad
+// page are zero-filled; each thread's copies of a ring slot end with an
+// arrival on the slot's barrier that fires when they land) into a ring of
+// 32 KB slots (two ckv pieces: one P.V accumulator's operand) plus one slot
+// for the rope piece.  A block's ckv pieces stay until its P.V is done; the
+// ring holds the first slot of the next block meanwhile.  Each thread also
+// prefetches one key's latent rows two blocks ahead into L2, so that the
+// copies issued as slots free up hit L2.
+//
+// Measured (GB300, 16 heads): an M=128 N=16 MMA issues about every 90
+// cycles, close to the N=128 rate, so a block's 68 MMAs take ~6k cycles; the
+// softmax (~2.5k cycles) and the refill of the slots a P.V frees sit between
+// them, and a block takes ~10k cycles (3.1 TB/s of latent rows at 64
+// requests).
+//
+// Invariance: block boundaries are absolute key positions, every head's
+// column of the MMAs is computed on its own, and the lazy-rescale decisions
+// and all reductions depend only on the request's own keys in a fixed order,
+// so a request's output bits do not depend on the batch.
 #include "bia_internal.h"
 #include "ptx.cuh"
 
@@ -24,284 +61,418 @@ namespace bia {
 
 namespace {
 
-constexpr int kDc = kMlaCkvDim;  // 512
-constexpr int kDp = kMlaKpeDim;  // 64
-constexpr int kMWarps = 8;       // consumer warps
-constexpr int kMThreads = (kMWarps + 1) * 32;
-constexpr int kMChunk = 8;       // keys per stage
-constexpr int kMGroup = 4;       // keys whose scores are reduced together
-constexpr int kMStages = 6;
-constexpr float kMLazy = 8.0f;   // log2 units
+constexpr int kHg = kMlaHeadGroup;           // 16 heads: the MMA's N
+constexpr int kKeys = 128;                   // keys per block: the MMA's M
+constexpr int kPiece = kKeys * 128;          // 128 rows x 64 bf16, SW128
+constexpr int kCkvPieces = kMlaCkvDim / 64;  // 8
+constexpr int kPairs = 5;                    // ring slots of two ckv pieces
+constexpr int kThreadsT = 288;
+constexpr int kMmaWarpT = 4;
+constexpr int kProdWarpT = 5;      // warps 5-8 copy the latent rows
+constexpr float kLazyT = 8.0f; // log2 units
 
-struct MlaSmem {
-  static constexpr int kCkvRow = kDc * 2;                        // 1024 bytes
-  static constexpr int kKpeRow = kDp * 2;                        // 128 bytes
-  static constexpr int kStage = kMChunk * (kCkvRow + kKpeRow);   // ckv rows then kpe rows
-  static constexpr int kBar = kMStages * kStage;
-  static constexpr int kFull = 0, kEmpty = kMStages, kNumBars = 2 * kMStages;
-  static constexpr int kBytes = kBar + kNumBars * 8;
-  static constexpr int kAlloc = kBytes + 128;
+struct TcSmem {
+  static constexpr int kQPiece = kHg * 128;           // 16 heads x 64 columns
+  static constexpr int kQ = 0;                         // 9 q pieces (8 ckv + rope)
+  static constexpr int kP = kQ + 9 * kQPiece;          // P: 128 keys x 128-byte rows
+  static constexpr int kRing = kP + kPiece;            // kPairs slots of 2 pieces
+  static constexpr int kKpe = kRing + kPairs * 2 * kPiece;
+  static constexpr int kBar = kKpe + kPiece;
+  static constexpr int bQFull = 0, bPairFull = 1, bPairEmpty = 1 + kPairs,
+                       bKpeFull = 1 + 2 * kPairs, bKpeEmpty = bKpeFull + 1, bSFull = bKpeEmpty + 1,
+                       bPFull = bSFull + 1, bPVDone = bPFull + 1, kNumBars = bPVDone + 1;
+  static constexpr int kRed = kBar + 256;              // float [2][4 warps][16 heads]
+  static constexpr int kLred = kRed + 2 * 4 * kHg * 4; // float [4 warps][16 heads]
+  static constexpr int kSlot = kLred + 4 * kHg * 4;
+  static constexpr int kBytes = kSlot + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kNumBars * 8 <= 256, "barrier area");
+  static_assert(kAlloc <= 232448, "shared memory per CTA");
 };
 
-__device__ __forceinline__ uint4 lds128m(uint32_t addr) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "r"(addr));
-  return r;
-}
-__device__ __forceinline__ uint32_t lds32m(uint32_t addr) {
-  uint32_t r;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
-  return r;
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
 }
 
-// HPW: heads per consumer warp (1 or 2); the CTA takes 8 * HPW heads.
-template <int HPW>
-__global__ void __launch_bounds__(kMThreads, 1) mla_decode_kernel(const AttnArgs a) {
-  using L = MlaSmem;
-  constexpr int HG = kMWarps * HPW;
+__global__ void __launch_bounds__(kThreadsT, 1)
+    mla_decode_tc_kernel(const __grid_constant__ AttnArgs a) {
+  using L = TcSmem;
+  constexpr uint32_t kIdescS = idesc_bf16_ab(128, kHg, false, false);
+  constexpr uint32_t kIdescPV = idesc_bf16_ab(128, kHg, true, true);
+  constexpr uint32_t kTmemCols = 128;
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) { return sbase + L::kBar + 8u * static_cast<uint32_t>(i); };
-  auto sCkv = [&](int st) { return sbase + st * L::kStage; };
-  auto sKpe = [&](int st) { return sbase + st * L::kStage + kMChunk * L::kCkvRow; };
+  auto pair_slot = [&](int s) { return sbase + L::kRing + static_cast<uint32_t>(s) * 2 * kPiece; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kSlot);
 
-  const int n_groups = a.Hq / HG;
-  const int64_t unit = blockIdx.x / n_groups;
-  const int hg = static_cast<int>(blockIdx.x - unit * n_groups);
+  // block = unit * head groups + head group: a unit's head groups run side by side
+  const int n_hg = (a.Hq + kHg - 1) / kHg;
+  const int64_t unit = blockIdx.x / n_hg;
+  const int hg = static_cast<int>(blockIdx.x - unit * n_hg);
   if (unit >= a.n_units) return;
   const Unit u = a.units[unit];
   if (u.b < 0) return;
   const ReqInfo r = a.reqs[u.b];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t key_begin = u.split * a.split;
   const int32_t key_end = min(key_begin + a.split, r.kv_len);
-  const int n_chunks = (key_end - key_begin + kMChunk - 1) / kMChunk;
+  const int nb = key_end > key_begin ? (key_end - key_begin + kKeys - 1) / kKeys : 0;
+  const int h_real = min(kHg, a.Hq - hg * kHg); // heads of this group (the rest are padding)
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kMStages; ++s) {
-      mbar_init(bar(L::kFull + s), 1);
-      mbar_init(bar(L::kEmpty + s), kMWarps);
+  if (warp == kMmaWarpT) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (tid == 0) {
+    mbar_init(bar(L::bQFull), 1);
+    for (int s = 0; s < kPairs; ++s) {
+      mbar_init(bar(L::bPairFull + s), 128); // one arrival per producer thread
+      mbar_init(bar(L::bPairEmpty + s), 1);
     }
+    mbar_init(bar(L::bKpeFull), 128);
+    mbar_init(bar(L::bKpeEmpty), 1);
+    mbar_init(bar(L::bSFull), 1);
+    mbar_init(bar(L::bPFull), 4); // one arrival per softmax warp
+    mbar_init(bar(L::bPVDone), 1);
     fence_mbar_init();
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // TMEM columns: S^T [0,16) (lanes = keys), O^T of latent columns
+  // 128*mb .. 128*mb+127 at [32+16mb, 48+16mb) (lanes = latent columns)
+  const uint32_t tS = tmem;
+  auto tO = [&](int mb) { return tmem + 32u + 16u * static_cast<uint32_t>(mb); };
 
-  if (warp == kMWarps) {
-    // ---------------------------------------------------------- producer
-    // lanes 0-7: the ckv rows of the stage's 8 keys, 8-15: their kpe rows;
-    // keys past the split or on a bad page are zero-filled instead
-    const int kl = lane & 7;
+  if (warp >= kProdWarpT) {
+    // ------------------------------------------------------------ producers
+    const int pt = tid - kProdWarpT * 32; // 0..127
+    const int32_t q_row = r.q_start * a.Hq + hg * kHg; // rows past B*H read as zeros
+    if (pt == 0 && nb > 0) {
+      mbar_expect_tx(bar(L::bQFull), 9u * L::kQPiece);
+      for (int p = 0; p < kCkvPieces; ++p)
+        tma_load_2d(sbase + L::kQ + p * L::kQPiece, &a.tm_q, 64 * p, q_row, bar(L::bQFull));
+      tma_load_2d(sbase + L::kQ + kCkvPieces * L::kQPiece, &a.tm_qpe, 0, q_row, bar(L::bQFull));
+    }
+    // Thread pt copies 16-byte chunk cc of keys kb, kb+8, ..., kb+120 of every
+    // block: of each pair's 256 bytes per key, and (cc < 8) of the rope row;
+    // its 16 page indices are fetched a block ahead.  Each copy group ends
+    // with an arrival that fires when the thread's copies have landed (full
+    // barriers count the 128 threads).  Thread pt also prefetches key pt's
+    // latent rows two blocks ahead into L2, its page index fetched a block
+    // before that.
+    const int cc = pt & 15, kb = pt >> 4;
     const int page_mask = (1 << a.page_shift) - 1;
-    for (int i = 0; i < n_chunks; ++i) {
-      const int st = i % kMStages;
-      if (i >= kMStages &&
-          !mbar_wait(bar(L::kEmpty + st), (i / kMStages - 1) & 1, a.status))
-        break;
-      const int32_t key = key_begin + i * kMChunk + kl;
-      bool ok = lane < 16 && key < key_end;
-      int32_t pg = 0;
-      if (ok) {
-        pg = __ldg(a.kv_indices + r.page_base + (key >> a.page_shift));
-        if (pg < 0 || pg >= a.num_pages) {
-          atomicOr(a.status, kStatusBadPage);
-          ok = false;
+    auto page_at = [&](int j, int k) -> int32_t {
+      const int32_t key = key_begin + j * kKeys + k;
+      return (j < nb && key < key_end)
+                 ? __ldg(a.kv_indices + r.page_base + (key >> a.page_shift)) : -1;
+    };
+    auto fetch = [&](int j, int32_t (&pg)[16]) {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) pg[n] = page_at(j, kb + 8 * n);
+    };
+    auto prefetch_rows = [&](int j, int32_t pg) {
+      const int32_t key = key_begin + j * kKeys + pt;
+      if (pg < 0 || pg >= a.num_pages) return;
+      const int64_t row = (static_cast<int64_t>(pg) << a.page_shift) + (key & page_mask);
+      prefetch_l2(a.k_cache + row * kMlaCkvDim, kMlaCkvDim * 2);
+      prefetch_l2(a.kpe_cache + row * kMlaKpeDim, kMlaKpeDim * 2);
+    };
+    prefetch_rows(1, page_at(1, pt));
+    int32_t pf_pg = page_at(2, pt);
+    const uint32_t swz = static_cast<uint32_t>(((cc & 7) ^ (kb & 7)) << 4); // key & 7 == kb & 7
+    int32_t pg_next[16];
+    fetch(0, pg_next);
+    bool ok = true;
+    for (int j = 0; j < nb && ok; ++j) {
+      prefetch_rows(j + 2, pf_pg);
+      pf_pg = page_at(j + 3, pt);
+      int32_t rows[16]; // latent row of each of this thread's keys; -1: zeros
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        const int32_t key = key_begin + j * kKeys + kb + 8 * n;
+        rows[n] = -1;
+        if (key < key_end) {
+          if (pg_next[n] < 0 || pg_next[n] >= a.num_pages)
+            atomicOr(a.status, kStatusBadPage);
+          else
+            rows[n] = (pg_next[n] << a.page_shift) + (key & page_mask);
         }
       }
-      const bool is_ckv = lane < 8;
-      const uint32_t bytes = is_ckv ? L::kCkvRow : L::kKpeRow;
-      const uint32_t dst = is_ckv ? sCkv(st) + kl * L::kCkvRow : sKpe(st) + kl * L::kKpeRow;
-      if (lane < 16 && !ok) {
-        for (uint32_t b = 0; b < bytes; b += 16)
-          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + b), "r"(0) : "memory");
-      }
-      const unsigned okm = __ballot_sync(0xffffffffu, ok);
-      const uint32_t tx = __popc(okm & 0xffu) * L::kCkvRow + __popc(okm & 0xff00u) * L::kKpeRow;
-      fence_proxy_async(); // zero fills precede the stage's consumers' async view
-      __syncwarp();
-      if (lane == 0) mbar_expect_tx(bar(L::kFull + st), tx);
-      __syncwarp();
-      if (ok) {
-        const int64_t slot = (static_cast<int64_t>(pg) << a.page_shift) + (key & page_mask);
-        if (is_ckv)
-          bulk_g2s(dst, a.k_cache + slot * kDc, bytes, bar(L::kFull + st));
-        else
-          bulk_g2s(dst, a.kpe_cache + slot * kDp, bytes, bar(L::kFull + st));
+      fetch(j + 1, pg_next); // in flight while this block's copies are issued
+      // pair 0 (its slot frees first), the rope piece (free once the
+      // previous block's S is done), then pairs 1-3
+      for (int step = 0; step < kCkvPieces / 2 + 1 && ok; ++step) {
+        if (step == 1) {
+          if (j >= 1) {
+            ok = mbar_wait(bar(L::bKpeEmpty), (j - 1) & 1, a.status);
+            if (!ok) break;
+          }
+          if (cc < 8) {
+            const uint32_t dbase = sbase + L::kKpe + swz;
+            const uint16_t *src0 = a.kpe_cache + cc * 8;
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+              cp_async16(dbase + (kb + 8 * n) * 128,
+                         src0 + static_cast<int64_t>(max(rows[n], 0)) * kMlaKpeDim, rows[n] >= 0);
+          }
+          cp_async_arrive(bar(L::bKpeFull));
+          continue;
+        }
+        const int q = step == 0 ? 0 : step - 1;
+        const int c = 4 * j + q, s = c % kPairs;
+        if (c >= kPairs) {
+          ok = mbar_wait(bar(L::bPairEmpty + s), ((c / kPairs) - 1) & 1, a.status);
+          if (!ok) break;
+        }
+        const uint32_t dbase = pair_slot(s) + (cc >> 3) * kPiece + swz;
+        const uint16_t *src0 = a.k_cache + 128 * q + cc * 8;
+#pragma unroll
+        for (int n = 0; n < 16; ++n)
+          cp_async16(dbase + (kb + 8 * n) * 128,
+                     src0 + static_cast<int64_t>(max(rows[n], 0)) * kMlaCkvDim, rows[n] >= 0);
+        cp_async_arrive(bar(L::bPairFull + s));
       }
     }
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers
-  const int h0 = hg * HG + warp * HPW; // first head of this warp
-  const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2);
-  uint64_t qn[HPW][8], qp[HPW];
-  float m[HPW], l[HPW];
-  uint64_t o2[HPW][8];
+    cp_async_wait_all(); // no copy outlives the CTA
+  } else if (warp == kMmaWarpT) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = nb == 0 || mbar_wait(bar(L::bQFull), 0, a.status);
+      for (int j = 0; j < nb && ok; ++j) {
+        // S^T = C Q^T: the eight ckv pieces, then the rope piece
+        for (int q = 0; q < kCkvPieces / 2 && ok; ++q) {
+          const int c = 4 * j + q, s = c % kPairs;
+          ok = mbar_wait(bar(L::bPairFull + s), (c / kPairs) & 1, a.status);
+          if (!ok) break;
+          fence_proxy_async(); // the rows were written by cp.async (generic proxy)
+          tc_fence_after();
 #pragma unroll
-  for (int k = 0; k < HPW; ++k) {
-    const int64_t qrow = static_cast<int64_t>(r.q_start) * a.Hq + h0 + k;
-    const uint4 w0 = *reinterpret_cast<const uint4 *>(a.q + qrow * kDc + lane * 16);
-    const uint4 w1 = *reinterpret_cast<const uint4 *>(a.q + qrow * kDc + lane * 16 + 8);
-    const uint32_t wp = *reinterpret_cast<const uint32_t *>(a.q_pe + qrow * kDp + lane * 2);
-    qn[k][0] = fmul2(bf16x2_to_f32x2(w0.x), sc2);
-    qn[k][1] = fmul2(bf16x2_to_f32x2(w0.y), sc2);
-    qn[k][2] = fmul2(bf16x2_to_f32x2(w0.z), sc2);
-    qn[k][3] = fmul2(bf16x2_to_f32x2(w0.w), sc2);
-    qn[k][4] = fmul2(bf16x2_to_f32x2(w1.x), sc2);
-    qn[k][5] = fmul2(bf16x2_to_f32x2(w1.y), sc2);
-    qn[k][6] = fmul2(bf16x2_to_f32x2(w1.z), sc2);
-    qn[k][7] = fmul2(bf16x2_to_f32x2(w1.w), sc2);
-    qp[k] = fmul2(bf16x2_to_f32x2(wp), sc2);
-    m[k] = -INFINITY;
-    l[k] = 0.f;
+          for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o2[k][i] = 0;
-  }
-
-  bool failed = false;
-  for (int i = 0; i < n_chunks; ++i) {
-    const int st = i % kMStages;
-    if (!mbar_wait(bar(L::kFull + st), (i / kMStages) & 1, a.status)) {
-      failed = true;
-      break;
-    }
-    const int n_keys = min(kMChunk, key_end - (key_begin + i * kMChunk));
-    // keys in groups of kMGroup: the group's scores are reduced together (their
-    // shuffle chains overlap) and its max drives one lazy-rescale decision;
-    // rows past the split's end are zero-filled and left out
-    for (int k0 = 0; k0 < n_keys; k0 += kMGroup) {
-      float sc[HPW][kMGroup];
-#pragma unroll
-      for (int q = 0; q < kMGroup; ++q) {
-        const uint32_t row = sCkv(st) + (k0 + q) * L::kCkvRow + lane * 32;
-        const uint4 c0 = lds128m(row);
-        const uint4 c1 = lds128m(row + 16);
-        const uint64_t p2 = bf16x2_to_f32x2(lds32m(sKpe(st) + (k0 + q) * L::kKpeRow + lane * 4));
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int k = 0; k < HPW; ++k) {
-          uint64_t acc = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ffma2(acc, qn[k][e], bf16x2_to_f32x2(cw[e]));
-          ffma2(acc, qp[k], p2);
-          float x, y;
-          f32x2_split(acc, x, y);
-          sc[k][q] = x + y;
+            for (int kk = 0; kk < 4; ++kk) {
+              const int piece = 2 * q + h2;
+              mma_bf16_ss(tS, desc_sw128(pair_slot(s) + h2 * kPiece + kk * 32, 16, 1024),
+                          desc_sw128(sbase + L::kQ + piece * L::kQPiece + kk * 32, 16, 1024),
+                          kIdescS, (piece | kk) != 0 ? 1u : 0u);
+            }
         }
-      }
-      // butterfly sums over the warp: the same bits on every lane
+        if (!ok) break;
+        ok = mbar_wait(bar(L::bKpeFull), j & 1, a.status);
+        if (!ok) break;
+        fence_proxy_async();
+        tc_fence_after();
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tS, desc_sw128(sbase + L::kKpe + kk * 32, 16, 1024),
+                      desc_sw128(sbase + L::kQ + kCkvPieces * L::kQPiece + kk * 32, 16, 1024),
+                      kIdescS, 1u);
+        mma_commit(bar(L::bKpeEmpty));
+        mma_commit(bar(L::bSFull));
+        // O^T += C^T P^T, one accumulator per pair of ckv pieces
+        ok = mbar_wait(bar(L::bPFull), j & 1, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        // each pair is released as soon as its accumulator's MMAs are done
 #pragma unroll
-        for (int k = 0; k < HPW; ++k)
+        for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
+          const int c = 4 * j + mb, s = c % kPairs;
 #pragma unroll
-          for (int q = 0; q < kMGroup; ++q) sc[k][q] += __shfl_xor_sync(0xffffffffu, sc[k][q], off);
-      float pw[HPW][kMGroup];
-#pragma unroll
-      for (int k = 0; k < HPW; ++k) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kMGroup; ++q)
-          if (k0 + q < n_keys) mx = fmaxf(mx, sc[k][q]);
-        if (mx > m[k] + kMLazy || m[k] == -INFINITY) {
-          const float alpha = ex2(m[k] - mx); // 0 when m == -inf
-          l[k] *= alpha;
-          const uint64_t a2 = f32x2(alpha, alpha);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o2[k][e] = fmul2(o2[k][e], a2);
-          m[k] = mx;
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            mma_bf16_ss(tO(mb), desc_sw128(pair_slot(s) + kk * 2048, kPiece, 1024),
+                        desc_sw128(sbase + L::kP + kk * 2048, kPiece, 1024), kIdescPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::bPairEmpty + s));
         }
-#pragma unroll
-        for (int q = 0; q < kMGroup; ++q) {
-          pw[k][q] = k0 + q < n_keys ? ex2(sc[k][q] - m[k]) : 0.f;
-          l[k] += pw[k][q];
-        }
-      }
-      // P.V: the group's latent rows read again from shared memory
-#pragma unroll
-      for (int q = 0; q < kMGroup; ++q) {
-        const uint32_t row = sCkv(st) + (k0 + q) * L::kCkvRow + lane * 32;
-        const uint4 c0 = lds128m(row);
-        const uint4 c1 = lds128m(row + 16);
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int k = 0; k < HPW; ++k) {
-          const uint64_t pp = f32x2(pw[k][q], pw[k][q]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ffma2(o2[k][e], pp, bf16x2_to_f32x2(cw[e]));
-        }
+        mma_commit(bar(L::bPVDone));
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar(L::kEmpty + st));
-  }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = tid; // key of the block = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float *red = reinterpret_cast<float *>(smem + L::kRed);
+    float m[kHg], l[kHg];
+#pragma unroll
+    for (int h = 0; h < kHg; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+    bool failed = false;
+    for (int j = 0; j < nb; ++j) {
+      if (!mbar_wait(bar(L::bSFull), j & 1, a.status)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[kHg];
+      tmem_ld16(tS + lane_base, v);
+      tmem_wait_ld();
+      const bool valid = key_begin + j * kKeys + t < key_end;
+      float s[kHg];
+#pragma unroll
+      for (int h = 0; h < kHg; ++h)
+        s[h] = (valid && h < h_real) ? __uint_as_float(v[h]) * a.scale_log2 : -INFINITY;
+      // block max per head: over the warp, then the 4 warps (same value everywhere)
+      float *rd = red + (j & 1) * 4 * kHg;
+      float mine = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < kHg; ++h) {
+        const float wm = warp_max(s[h]);
+        mine = lane == h ? wm : mine;
+      }
+      if (lane < kHg) rd[warp * kHg + lane] = mine;
+      bar_sync_named(1, 128);
+      // lazy online softmax: the running max of a head moves only when the
+      // block max exceeds it by more than 2^8
+      float bmv[kHg];
+#pragma unroll
+      for (int h4 = 0; h4 < kHg / 4; ++h4) {
+        const float4 w0 = reinterpret_cast<const float4 *>(rd)[h4];
+        const float4 w1 = reinterpret_cast<const float4 *>(rd + kHg)[h4];
+        const float4 w2 = reinterpret_cast<const float4 *>(rd + 2 * kHg)[h4];
+        const float4 w3 = reinterpret_cast<const float4 *>(rd + 3 * kHg)[h4];
+        bmv[4 * h4 + 0] = fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x));
+        bmv[4 * h4 + 1] = fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y));
+        bmv[4 * h4 + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
+        bmv[4 * h4 + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
+      }
+      float alpha[kHg], p[kHg];
+      bool resc = false;
+#pragma unroll
+      for (int h = 0; h < kHg; ++h) {
+        const float bm = bmv[h];
+        alpha[h] = 1.f;
+        if (bm > m[h] + kLazyT || (m[h] == -INFINITY && bm != -INFINITY)) {
+          alpha[h] = ex2(m[h] - bm); // 0 when m == -inf
+          m[h] = bm;
+          resc = true;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kHg; ++h) {
+        const float ms = m[h] == -INFINITY ? 0.f : m[h];
+        p[h] = s[h] == -INFINITY ? 0.f : ex2(s[h] - ms);
+        l[h] = fmaf(l[h], alpha[h], p[h]);
+      }
+      // the previous P.V is done: P's buffer is free and O may be rescaled
+      if (j > 0 && !mbar_wait(bar(L::bPVDone), (j - 1) & 1, a.status)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      if (j > 0 && resc) { // resc is the same on every thread
+#pragma unroll
+        for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
+          uint32_t o[kHg];
+          tmem_ld16(tO(mb) + lane_base, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < kHg; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+          tmem_st16(tO(mb) + lane_base, o);
+        }
+        tmem_wait_st();
+      }
+      // P row of key t: heads 0-7 in 16-byte chunk 0, heads 8-15 in chunk 1
+      const uint32_t prow = sbase + L::kP;
+      sts128(prow + sw128(t, 0), make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
+                                            pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7])));
+      sts128(prow + sw128(t, 1), make_uint4(pack_bf16(p[8], p[9]), pack_bf16(p[10], p[11]),
+                                            pack_bf16(p[12], p[13]), pack_bf16(p[14], p[15])));
+      fence_proxy_async(); // P is read by the MMA (async proxy)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bPFull));
+    }
 
-  // epilogue: this warp's heads, one split: o = O / l, lse = (m + log2 l) ln 2
-  const bool single = (r.kv_len - 1) / a.split == 0;
+    // ---- epilogue: l = sum of every thread's partial sums (warp butterfly,
+    // then the 4 warps in order), o = O^T / l, lse = (m + log2 l) ln 2
+    const bool have = __all_sync(0xffffffffu, !failed && nb > 0 &&
+                                                  mbar_wait(bar(L::bPVDone), (nb - 1) & 1,
+                                                            a.status));
+    tc_fence_after();
 #pragma unroll
-  for (int k = 0; k < HPW; ++k) {
-    const int h = h0 + k;
-    const bool nonzero = !failed && l[k] > 0.f;
-    const float lse = nonzero ? __fmul_rn(__fadd_rn(m[k], lg2(l[k])), kLn2) : -INFINITY;
-    float o[16];
+    for (int h = 0; h < kHg; ++h)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f32x2_split(o2[k][e], o[2 * e], o[2 * e + 1]);
-    const int64_t row = static_cast<int64_t>(r.q_start) * a.Hq + h;
-    if (single) {
-      uint4 w[2];
+      for (int off = 16; off >= 1; off >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+    float *lr = reinterpret_cast<float *>(smem + L::kLred);
+    float lw = 0.f;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float v[8];
+    for (int h = 0; h < kHg; ++h) lw = lane == h ? l[h] : lw;
+    if (lane < kHg) lr[warp * kHg + lane] = lw;
+    bar_sync_named(1, 128);
+    float inv[kHg];
+    bool nz[kHg];
+    float lse_mine = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = nonzero ? __fdiv_rn(o[q * 8 + e], l[k]) : 0.f;
-        w[q] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
-                          pack_bf16(v[6], v[7]));
+    for (int h = 0; h < kHg; ++h) {
+      const float ls = __fadd_rn(__fadd_rn(__fadd_rn(lr[h], lr[kHg + h]), lr[2 * kHg + h]),
+                                 lr[3 * kHg + h]);
+      nz[h] = have && ls > 0.f;
+      inv[h] = nz[h] ? __frcp_rn(ls) : 0.f;
+      const float lse = nz[h] ? __fmul_rn(__fadd_rn(m[h], lg2(ls)), kLn2) : -INFINITY;
+      lse_mine = t == h ? lse : lse_mine;
+    }
+    const bool single = (r.kv_len - 1) / a.split == 0; // one split: the final row
+    const int64_t head0 = static_cast<int64_t>(r.q_start) * a.Hq + hg * kHg;
+    const int64_t prow0 = (r.rowbase + u.split) * a.Hq + hg * kHg;
+#pragma unroll
+    for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
+      uint32_t o[kHg];
+      if (have) {
+        tmem_ld16(tO(mb) + lane_base, o);
+        tmem_wait_ld();
       }
-      uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * kDc + lane * 16);
-      dst[0] = w[0];
-      dst[1] = w[1];
-      if (a.lse && lane == 0) a.lse[row] = lse;
-    } else {
-      const int64_t prow = (r.rowbase + u.split) * a.Hq + h;
-      float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * kDc + lane * 16);
+      const int d = mb * 128 + t; // latent column of this thread
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = nonzero ? __fdiv_rn(o[q * 4 + e], l[k]) : 0.f;
-        dst[q] = make_float4(v[0], v[1], v[2], v[3]);
+      for (int h = 0; h < kHg; ++h) {
+        if (h >= h_real) break;
+        const float val = nz[h] ? __fmul_rn(__uint_as_float(o[h]), inv[h]) : 0.f;
+        if (single)
+          a.out[(head0 + h) * kMlaCkvDim + d] = to_bf16(val);
+        else
+          a.part_o[(prow0 + h) * kMlaCkvDim + d] = val;
       }
-      if (lane == 0) a.part_lse[prow] = lse;
+    }
+    if (t < h_real) {
+      if (single) {
+        if (a.lse) a.lse[head0 + t] = lse_mine;
+      } else {
+        a.part_lse[prow0 + t] = lse_mine;
+      }
     }
   }
-}
 
-template <int HPW>
-cudaError_t launch_mla_hpw(const AttnArgs &a, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<HPW>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MlaSmem::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured = true;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarpT) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
-  const int64_t blocks = a.n_units * (a.Hq / (kMWarps * HPW));
-  if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
-  mla_decode_kernel<HPW><<<static_cast<unsigned>(blocks), kMThreads, MlaSmem::kAlloc, s>>>(a);
-  return cudaGetLastError();
 }
 
 } // namespace
 
 cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
-  // 16 heads per CTA when they divide evenly, else 8
-  return a.Hq % 16 == 0 ? launch_mla_hpw<2>(a, s) : launch_mla_hpw<1>(a, s);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TcSmem::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int64_t blocks = a.n_units * ((a.Hq + kHg - 1) / kHg);
+  if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
+  mla_decode_tc_kernel<<<static_cast<unsigned>(blocks), kThreadsT, TcSmem::kAlloc, s>>>(a);
+  return cudaGetLastError();
 }
 
 } // namespace bia

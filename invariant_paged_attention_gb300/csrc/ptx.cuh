@@ -82,6 +82,12 @@ __device__ __forceinline__ uint64_t ffma2r(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+// Maximum of x over the 32 lanes of the warp (every lane gets it).
+__device__ __forceinline__ float warp_max(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -139,6 +145,12 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global memory
+// into L2; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- bulk copy
 // Global -> shared bulk copy (TMA, no tensor map) of `bytes` (multiple of 16,
 // both addresses 16-byte aligned); completes `bytes` transactions on `bar`.
@@ -160,6 +172,16 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int3
   asm volatile("cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx"
                "::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
                "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+               : "memory");
+}
+
+// A 2-D tiled TMA load (column x, row y) into this CTA's shared memory,
+// completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile("cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+               "l"(tmap), "r"(x), "r"(y), "r"(bar)
                : "memory");
 }
 
@@ -357,6 +379,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with either operand MN-major (bit 15: A, bit 16: B).
+__host__ __device__ constexpr uint32_t idesc_bf16_ab(int M, int N, bool a_mn_major,
+                                                     bool b_mn_major) {
+  return idesc_bf16(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte
