@@ -60,6 +60,9 @@ def parse_args():
                    help="decode requests (the decode sweep's largest batch by default)")
     p.add_argument("--sweep", action="store_true",
                    help="time every workload (one JSON line each) instead of the default step")
+    p.add_argument("--sweep-only", default="",
+                   help="comma list of sweep groups to run (tiny,cfg2,append,cfg3,cfg5,d256,"
+                        "mla,cfg4); empty: all")
     return p.parse_args()
 
 
@@ -377,39 +380,68 @@ def run_sweep(args):
         line.update(extra or {})
         print(json.dumps(line), flush=True)
 
+    groups = {g for g in args.sweep_only.split(",") if g}
+    want = lambda g: not groups or g in groups  # noqa: E731
     D, Hq, Hkv = 128, 32, 8
     # prefill workloads
-    st = wl.cfg1_tiny(dev)
-    c = wl.whole_prefill(st)
-    cm, km = time_calls([prefill_fn(st, c)])
-    emit("cfg1 tiny prefill (256 tok, 4q/1kv, d64, page 16)", "prefill",
-         prefill_flops(c, 64, 4), cm, km)
-    st = wl.cfg2_prefill(dev)
-    c = wl.whole_prefill(st)
-    cm, km = time_calls([prefill_fn(st, c)])
-    emit("cfg2 batched prefill (8 req, U[512,8192])", "prefill", prefill_flops(c, D, Hq), cm, km)
-    k_new, v_new = wl.new_kv_rows(c)
-    cm, km = time_calls([append_fn(st, c, k_new, v_new)])
-    # read the new rows once, write them once
-    emit("paged-KV append of the cfg2 prompts (8 req, U[512,8192], page 1)", "append",
-         4 * k_new.numel() * k_new.element_size(), cm, km)
-    del st, c, k_new, v_new
-    st = wl.cfg3_prefix(dev)
-    whole = wl.whole_prefill(st)
-    cm, km = time_calls([prefill_fn(st, whole)])
-    fl = prefill_flops(whole, D, Hq)
-    emit("cfg3 prefix extend, unchunked (4 x 16384 new)", "prefill", fl, cm, km)
-    fns = [prefill_fn(st, cc) for cc in wl.chunked_calls(st, 256)]
-    cm, _ = time_calls(fns)
-    emit("cfg3 prefix extend, 64 chunks of 256", "prefill", fl, cm, None)
-    del st, whole, fns
+    if want("tiny"):
+        st = wl.cfg1_tiny(dev)
+        c = wl.whole_prefill(st)
+        cm, km = time_calls([prefill_fn(st, c)])
+        emit("cfg1 tiny prefill (256 tok, 4q/1kv, d64, page 16)", "prefill",
+             prefill_flops(c, 64, 4), cm, km)
+    if want("cfg2") or want("append"):
+        st = wl.cfg2_prefill(dev)
+        c = wl.whole_prefill(st)
+        if want("cfg2"):
+            cm, km = time_calls([prefill_fn(st, c)])
+            emit("cfg2 batched prefill (8 req, U[512,8192])", "prefill", prefill_flops(c, D, Hq),
+                 cm, km)
+        if want("append"):
+            k_new, v_new = wl.new_kv_rows(c)
+            cm, km = time_calls([append_fn(st, c, k_new, v_new)])
+            # read the new rows once, write them once
+            emit("paged-KV append of the cfg2 prompts (8 req, U[512,8192], page 1)", "append",
+                 4 * k_new.numel() * k_new.element_size(), cm, km)
+            del k_new, v_new
+        del st, c
+    if want("cfg3"):
+        st = wl.cfg3_prefix(dev)
+        whole = wl.whole_prefill(st)
+        cm, km = time_calls([prefill_fn(st, whole)])
+        fl = prefill_flops(whole, D, Hq)
+        emit("cfg3 prefix extend, unchunked (4 x 16384 new)", "prefill", fl, cm, km)
+        fns = [prefill_fn(st, cc) for cc in wl.chunked_calls(st, 256)]
+        cm, _ = time_calls(fns)
+        emit("cfg3 prefix extend, 64 chunks of 256", "prefill", fl, cm, None)
+        del st, whole, fns
+    if want("cfg5"):
+        sweep_cfg5(wl, dev, D, Hq, Hkv, time_calls, prefill_fn, decode_fn, emit, prefill_flops,
+                   kv_bytes)
+    if want("d256"):
+        sweep_d256(wl, dev, time_calls, prefill_fn, decode_fn, emit, prefill_flops, kv_bytes)
+    if want("mla"):
+        sweep_mla(wl, bia, dev, stream, time_calls, emit)
+    if want("cfg4"):
+        for B in (1, 8, 64, 256):
+            st = wl.cfg4_decode(dev, B)
+            c = wl.whole_prefill(st)
+            cm, km = time_calls([decode_fn(st, c)])
+            emit(f"cfg4 decode B={B} (ctx U[1024,32768], page 1)", "decode", kv_bytes(c, Hkv, D),
+                 cm, km)
+            del st, c
+            torch.cuda.empty_cache()
+
+
+def sweep_cfg5(wl, dev, D, Hq, Hkv, time_calls, prefill_fn, decode_fn, emit, prefill_flops,
+               kv_bytes):
     pst, dst = wl.cfg5_mixed(dev)
     pc = wl.whole_prefill(pst)
     cm, km = time_calls([prefill_fn(pst, pc)])
     emit("cfg5 mixed prefill call (4096-tok chunk + 64 one-token extends, page 16)", "prefill",
          prefill_flops(pc, D, Hq), cm, km, {"kv_bytes": kv_bytes(pc, Hkv, D)})
     # its two parts on their own: the chunk (tensor bound) and the one-token
-    # extends (K/V streaming through the prefill kernel)
+    # extends (their single-token q tiles streamed by the decode kernel)
     chunk = wl.make_call(pst, [(0, 0, pst.seqs[0].new)])
     cm, km = time_calls([prefill_fn(pst, chunk)])
     emit("cfg5 chunk alone (4096 new tokens after a 4096-token prefix, page 16)", "prefill",
@@ -423,6 +455,9 @@ def run_sweep(args):
     emit("cfg5 decodes (32 x 131072 ctx, page 16)", "decode", kv_bytes(dc, Hkv, D), cm, km)
     del pst, dst, pc, dc
     torch.cuda.empty_cache()
+
+
+def sweep_d256(wl, dev, time_calls, prefill_fn, decode_fn, emit, prefill_flops, kv_bytes):
     # head_dim 256 (16 q / 8 kv heads): the wide prefill kernel and decode
     st = wl.wide_prefill(dev)
     c = wl.whole_prefill(st)
@@ -437,6 +472,9 @@ def run_sweep(args):
          kv_bytes(c, 8, 256), cm, km)
     del st, c
     torch.cuda.empty_cache()
+
+
+def sweep_mla(wl, bia, dev, stream, time_calls, emit):
     # multi-head latent attention decode: 16 heads over one 512 + 64 latent cache
     ctx = wl.uniform_lengths(64, 1024, 32768, 4000)
     mst = wl.MLAStore([wl.Sequence(7700 + i, c - 1, 1) for i, c in enumerate(ctx)], 16, 512, 64,
@@ -461,14 +499,6 @@ def run_sweep(args):
          sum(mc.kv_lens) * (512 + 64) * 2, cm, km)
     del mst, mc, mws, mout
     torch.cuda.empty_cache()
-    for B in (1, 8, 64, 256):
-        st = wl.cfg4_decode(dev, B)
-        c = wl.whole_prefill(st)
-        cm, km = time_calls([decode_fn(st, c)])
-        emit(f"cfg4 decode B={B} (ctx U[1024,32768], page 1)", "decode", kv_bytes(c, Hkv, D), cm,
-             km)
-        del st, c
-        torch.cuda.empty_cache()
 
 
 def main():
