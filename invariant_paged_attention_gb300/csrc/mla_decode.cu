@@ -320,6 +320,14 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       for (int h = 0; h < kHg; ++h)
         s[h] = (valid && h < h_real) ? __uint_as_float(v[h]) * a.scale_log2 : -INFINITY;
       // block max per head: over the warp, then the 4 warps (same value everywhere)
+      // P against the running max, computed while the block max is exchanged
+      // (the running max rarely moves: then these are the final values)
+      float p[kHg];
+#pragma unroll
+      for (int h = 0; h < kHg; ++h) {
+        const float ms = m[h] == -INFINITY ? 0.f : m[h];
+        p[h] = s[h] == -INFINITY ? 0.f : ex2(s[h] - ms);
+      }
       float *rd = red + (j & 1) * 4 * kHg;
       float mine = -INFINITY;
 #pragma unroll
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       if (lane < kHg) rd[warp * kHg + lane] = mine;
       bar_sync_named(1, 128);
       // lazy online softmax: the running max of a head moves only when the
-      // block max exceeds it by more than 2^8
+      // block max exceeds it by more than 2^8; such a head's P is recomputed
       float bmv[kHg];
 #pragma unroll
       for (int h4 = 0; h4 < kHg / 4; ++h4) {
@@ -343,24 +351,26 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         bmv[4 * h4 + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
         bmv[4 * h4 + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
       }
-      float alpha[kHg], p[kHg];
-      bool resc = false;
+      uint32_t up = 0; // heads whose running max moves (the same on every thread)
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) {
-        const float bm = bmv[h];
-        alpha[h] = 1.f;
-        if (bm > m[h] + kLazyT || (m[h] == -INFINITY && bm != -INFINITY)) {
-          alpha[h] = ex2(m[h] - bm); // 0 when m == -inf
-          m[h] = bm;
-          resc = true;
+      for (int h = 0; h < kHg; ++h)
+        if (bmv[h] > m[h] + kLazyT || (m[h] == -INFINITY && bmv[h] != -INFINITY)) up |= 1u << h;
+      float alpha[kHg];
+#pragma unroll
+      for (int h = 0; h < kHg; ++h) alpha[h] = 1.f;
+      const bool resc = up != 0;
+      if (resc) {
+#pragma unroll
+        for (int h = 0; h < kHg; ++h) {
+          if ((up >> h) & 1u) {
+            alpha[h] = ex2(m[h] - bmv[h]); // 0 when m == -inf
+            m[h] = bmv[h];
+            p[h] = s[h] == -INFINITY ? 0.f : ex2(s[h] - m[h]);
+          }
         }
       }
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) {
-        const float ms = m[h] == -INFINITY ? 0.f : m[h];
-        p[h] = s[h] == -INFINITY ? 0.f : ex2(s[h] - ms);
-        l[h] = fmaf(l[h], alpha[h], p[h]);
-      }
+      for (int h = 0; h < kHg; ++h) l[h] = fmaf(l[h], alpha[h], p[h]);
       // the previous P.V is done: P's buffer is free and O may be rescaled
       if (j > 0 && !mbar_wait(bar(L::bPVDone), (j - 1) & 1, a.status)) {
         failed = true;
