@@ -71,7 +71,7 @@ constexpr int kMmaWarpT = 4;
 constexpr int kProdWarpT = 5;      // warps 5-8 copy the latent rows
 constexpr float kLazyT = 8.0f; // log2 units
 
-struct TcSmem {
+struct MlaSmem {
   static constexpr int kQPiece = kHg * 128;           // 16 heads x 64 columns
   static constexpr int kQ = 0;                         // 9 q pieces (8 ckv + rope)
   static constexpr int kP = kQ + 9 * kQPiece;          // P: 128 keys x 128-byte rows
@@ -97,8 +97,8 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 }
 
 __global__ void __launch_bounds__(kThreadsT, 1)
-    mla_decode_tc_kernel(const __grid_constant__ AttnArgs a) {
-  using L = TcSmem;
+    mla_decode_kernel(const __grid_constant__ AttnArgs a) {
+  using L = MlaSmem;
   constexpr uint32_t kIdescS = idesc_bf16_ab(128, kHg, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_ab(128, kHg, true, true);
   constexpr uint32_t kTmemCols = 128;
@@ -473,15 +473,15 @@ cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcSmem::kAlloc);
+                                         MlaSmem::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int64_t blocks = a.n_units * ((a.Hq + kHg - 1) / kHg);
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
-  mla_decode_tc_kernel<<<static_cast<unsigned>(blocks), kThreadsT, TcSmem::kAlloc, s>>>(a);
+  mla_decode_kernel<<<static_cast<unsigned>(blocks), kThreadsT, MlaSmem::kAlloc, s>>>(a);
   return cudaGetLastError();
 }
 
