@@ -80,3 +80,69 @@ def test_captured_prefill_and_decode_replay_bit_identically():
         assert same_bits(g[0], e_pout) and same_bits(g[1], e_plse)
         assert same_bits(g[2], e_dout) and same_bits(g[3], e_dlse)
         assert torch.isfinite(g[0].float()).all()
+
+
+def test_captured_append_extend_and_mla_replay_bit_identically():
+    """An append, then an extend whose single-token q tiles run on the
+    streaming kernel, then an MLA decode, captured as one graph: replays with
+    new inputs match eager calls bit for bit."""
+    store = wl.PagedStore([wl.Sequence(8300 + i, p, n) for i, (p, n) in
+                           enumerate([(700, 33), (5000, 1), (0, 64)])], 32, 8, 128, 16, DEV,
+                          layout_seed=83)
+    call = wl.whole_prefill(store)
+    desc = bia.make_desc(32, 8, 128, 16)
+    k_new, v_new = wl.new_kv_rows(call)
+    k_new, v_new = k_new.clone(), v_new.clone()
+    idx = [call.qo_indptr.to(DEV), call.kv_indptr.to(DEV), call.kv_indices.to(DEV),
+           call.kv_last_page_len.to(DEV)]
+    ws = torch.empty(bia.bia_prefill_workspace_size(desc, call.qo_indptr, call.kv_indptr,
+                                                    call.kv_last_page_len),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(call.q)
+    lse = torch.empty(call.total_q, 32, dtype=torch.float32, device=DEV)
+    q = call.q.clone()
+
+    mst = wl.MLAStore([wl.Sequence(8400 + i, c - 1, 1) for i, c in enumerate([3000, 129, 5000])],
+                      16, 512, 64, 16, DEV, layout_seed=84)
+    mc = wl.mla_call(mst, [(i, 0, 1) for i in range(3)])
+    mdesc = bia.make_mla_desc(16, 16)
+    mws = torch.empty(bia.bia_mla_decode_workspace_size(mdesc, mc.kv_indptr, mc.kv_last_page_len),
+                      dtype=torch.uint8, device=DEV)
+    mout = torch.empty((3, 16, 512), dtype=torch.bfloat16, device=DEV)
+    mlse = torch.empty((3, 16), dtype=torch.float32, device=DEV)
+    midx = [mc.kv_indptr.to(DEV), mc.kv_indices.to(DEV), mc.kv_last_page_len.to(DEV)]
+    q_nope, q_pe = mc.q_nope.clone(), mc.q_pe.clone()
+
+    def step(stream=None):
+        bia.bia_append_paged_kv(desc, k_new, v_new, store.k_cache, store.v_cache, *idx,
+                                call.qo_indptr, call.kv_indptr, call.kv_last_page_len,
+                                stream=stream)
+        bia.bia_prefill_paged(desc, q, store.k_cache, store.v_cache, *idx, call.qo_indptr,
+                              call.kv_indptr, call.kv_last_page_len, ws, out, lse, stream=stream)
+        bia.bia_mla_decode_paged(mdesc, q_nope, q_pe, mst.ckv_cache, mst.kpe_cache, *midx,
+                                 mc.kv_indptr, mc.kv_last_page_len, mws, mout, mlse,
+                                 stream=stream)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        step(stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(stream=torch.cuda.current_stream())
+
+    for trial in range(2):
+        q.copy_(wl.draw_normal_bf16(q.shape, 9300 + trial, DEV))
+        k_new.copy_(wl.draw_normal_bf16(k_new.shape, 9400 + trial, DEV))
+        v_new.copy_(wl.draw_normal_bf16(v_new.shape, 9500 + trial, DEV))
+        q_nope.copy_(wl.draw_normal_bf16(q_nope.shape, 9600 + trial, DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        g = [t.clone() for t in (out, lse, mout, mlse)]
+        step()
+        torch.cuda.synchronize()
+        assert same_bits(g[0], out) and same_bits(g[1], lse)
+        assert same_bits(g[2], mout) and same_bits(g[3], mlse)
+        assert torch.isfinite(g[0].float()).all() and torch.isfinite(g[2].float()).all()
