@@ -231,61 +231,102 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
       break;
     }
     const int32_t key0 = key_begin + (warp + kWarps * i) * kChunk;
+    if constexpr (kOwnHead) {
+      // the chunk's scores first (this lane: head sub/4 of key s*KPW + grp),
+      // then one lazy-rescale decision per chunk and head (the chunk max over
+      // both key groups of the warp), then P.V
+      float c[STEPS];
+      bool vld[STEPS];
 #pragma unroll
-    for (int s = 0; s < STEPS; ++s) {
-      const int kl = s * KPW + grp; // row of the chunk
-      const uint4 kw = lds128(sK(st) + kl * L::kRow + sub * 16);
-      const uint4 vw = lds128(sV(st) + kl * L::kRow + sub * 16);
-      const uint64_t k2[4] = {bf16x2_to_f32x2(kw.x), bf16x2_to_f32x2(kw.y),
-                              bf16x2_to_f32x2(kw.z), bf16x2_to_f32x2(kw.w)};
-      float sc[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        uint64_t acc = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ffma2(acc, q2[g][k], k2[k]);
-        float x, y;
-        f32x2_split(acc, x, y);
-        sc[g] = x + y;
-      }
-      bool valid = key0 + kl < key_end; // past the split's last key: no weight
-      if constexpr (MASK) {
-        const int64_t bit = mask_row + key0 + kl;
-        valid = valid && ((__ldg(a.mask + (bit >> 5)) >> (bit & 31)) & 1u);
-      }
-      const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
-                              bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
-      if constexpr (kOwnHead) {
-        // each lane runs the online softmax of head sub/4 only; the weights of
-        // the four heads are then gathered for P.V
-        const float c = reduce_scatter4(sc);
-        const bool resc = valid && (c > m[0] + kLazyThreshold || m[0] == -INFINITY);
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ex2(m[0] - c);
-          l[0] *= alpha;
-          m[0] = c;
-        }
-        const float p = valid ? ex2(c - m[0]) : 0.f;
-        l[0] += p;
-        const int base = lane & ~15;
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float ag = __shfl_sync(0xffffffffu, alpha, base + 4 * g);
-            const uint64_t a2 = f32x2(ag, ag);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
-          }
-        }
+      for (int s = 0; s < STEPS; ++s) {
+        const int kl = s * KPW + grp; // row of the chunk
+        const uint4 kw = lds128(sK(st) + kl * L::kRow + sub * 16);
+        const uint64_t k2[4] = {bf16x2_to_f32x2(kw.x), bf16x2_to_f32x2(kw.y),
+                                bf16x2_to_f32x2(kw.z), bf16x2_to_f32x2(kw.w)};
+        float sc[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float pg = __shfl_sync(0xffffffffu, p, base + 4 * g);
+          uint64_t acc = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ffma2(acc, q2[g][k], k2[k]);
+          float x, y;
+          f32x2_split(acc, x, y);
+          sc[g] = x + y;
+        }
+        c[s] = reduce_scatter4(sc);
+        bool valid = key0 + kl < key_end; // past the split's last key: no weight
+        if constexpr (MASK) {
+          const int64_t bit = mask_row + key0 + kl;
+          valid = valid && ((__ldg(a.mask + (bit >> 5)) >> (bit & 31)) & 1u);
+        }
+        vld[s] = valid;
+      }
+      float cm = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < STEPS; ++s) cm = vld[s] ? fmaxf(cm, c[s]) : cm;
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16)); // lanes l and l^16: the same head
+      const bool resc = cm > m[0] + kLazyThreshold || (m[0] == -INFINITY && cm != -INFINITY);
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2(m[0] - cm); // 0 when m == -inf
+        l[0] *= alpha;
+        m[0] = cm;
+      }
+      const int base = lane & ~15;
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float ag = __shfl_sync(0xffffffffu, alpha, base + 4 * g);
+          const uint64_t a2 = f32x2(ag, ag);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
+        }
+      }
+      float p[STEPS];
+#pragma unroll
+      for (int s = 0; s < STEPS; ++s) {
+        p[s] = vld[s] ? ex2(c[s] - m[0]) : 0.f;
+        l[0] += p[s];
+      }
+#pragma unroll
+      for (int s = 0; s < STEPS; ++s) {
+        const int kl = s * KPW + grp;
+        const uint4 vw = lds128(sV(st) + kl * L::kRow + sub * 16);
+        const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
+                                bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pg = __shfl_sync(0xffffffffu, p[s], base + 4 * g);
           const uint64_t p2 = f32x2(pg, pg);
 #pragma unroll
           for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
         }
-      } else {
+      }
+    } else {
+#pragma unroll
+      for (int s = 0; s < STEPS; ++s) {
+        const int kl = s * KPW + grp; // row of the chunk
+        const uint4 kw = lds128(sK(st) + kl * L::kRow + sub * 16);
+        const uint4 vw = lds128(sV(st) + kl * L::kRow + sub * 16);
+        const uint64_t k2[4] = {bf16x2_to_f32x2(kw.x), bf16x2_to_f32x2(kw.y),
+                                bf16x2_to_f32x2(kw.z), bf16x2_to_f32x2(kw.w)};
+        float sc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          uint64_t acc = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ffma2(acc, q2[g][k], k2[k]);
+          float x, y;
+          f32x2_split(acc, x, y);
+          sc[g] = x + y;
+        }
+        bool valid = key0 + kl < key_end; // past the split's last key: no weight
+        if constexpr (MASK) {
+          const int64_t bit = mask_row + key0 + kl;
+          valid = valid && ((__ldg(a.mask + (bit >> 5)) >> (bit & 31)) & 1u);
+        }
+        const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
+                                bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
         group_reduce<G, LPK>(sc);
         // online softmax with lazy rescale: the running max moves only when a
         // score exceeds it by more than 2^8 (a function of this lane group's
