@@ -13,7 +13,11 @@
 // fp32x2 FMAs.  Every lane group keeps an online softmax per head over its own
 // keys (a fixed function of the key index), rescaled lazily when its max grows
 // by more than 2^8; lane groups and then warps are combined in a fixed order,
-// so a request's partial and output have the same bits in any batch.
+// so a request's partial and output have the same bits in any batch.  For 4
+// heads of 128 columns (16 lanes a key) a chunk's 8 scores are computed first
+// and the rescale is decided once per chunk and head, on the chunk max: the
+// per-key compare, vote and branch were most of the non-FMA instructions of a
+// stream that is issue-bound.
 //
 // The same kernel streams the single-token q tiles of a prefill call (a
 // one-token extend, or a request's one-token tail tile) with the prefill
