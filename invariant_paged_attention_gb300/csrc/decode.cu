@@ -17,8 +17,8 @@
 // heads of 128 columns (16 lanes a key) a chunk's 8 scores are computed first
 // and the rescale is decided once per chunk and head, on the chunk max: the
 // per-key compare, vote and branch were most of the non-FMA instructions of a
-// stream that is issue-bound.  Other shapes do the same when a chunk's scores
-// fit in 16 registers per lane, else decide per key.
+// stream that is issue-bound.  Other shapes do the same per chunk, or per
+// sub-chunk when a chunk's scores would not fit in 16 registers per lane.
 //
 // The same kernel streams the single-token q tiles of a prefill call (a
 // one-token extend, or a request's one-token tail tile) with the prefill
@@ -122,8 +122,10 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
   // lanes 4h..4h+3 of each lane group (m[0], l[0]); otherwise every lane keeps
   // all G states
   constexpr bool kOwnHead = (G == 4 && LPK == 16);
-  // a chunk's scores fit in registers: one rescale decision per chunk
-  constexpr bool kChunkSoftmax = STEPS * G <= 16;
+  // steps whose scores share one rescale decision: the whole chunk when its
+  // scores fit in 16 registers per lane
+  constexpr int SUB = STEPS * G <= 16 ? STEPS : 16 / G;
+  static_assert(STEPS % SUB == 0, "sub-chunks");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -309,111 +311,67 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
           for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
         }
       }
-    } else if constexpr (kChunkSoftmax) {
-      // as above with every lane holding all G scores: the chunk's scores,
-      // one rescale decision per chunk and head, then P.V
-      float sc[STEPS][G];
-      bool vld[STEPS];
-#pragma unroll
-      for (int s = 0; s < STEPS; ++s) {
-        const int kl = s * KPW + grp; // row of the chunk
-        const uint4 kw = lds128(sK(st) + kl * L::kRow + sub * 16);
-        const uint64_t k2[4] = {bf16x2_to_f32x2(kw.x), bf16x2_to_f32x2(kw.y),
-                                bf16x2_to_f32x2(kw.z), bf16x2_to_f32x2(kw.w)};
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          uint64_t acc = 0;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) ffma2(acc, q2[g][k], k2[k]);
-          float x, y;
-          f32x2_split(acc, x, y);
-          sc[s][g] = x + y;
-        }
-        group_reduce<G, LPK>(sc[s]);
-        bool valid = key0 + kl < key_end; // past the split's last key: no weight
-        if constexpr (MASK) {
-          const int64_t bit = mask_row + key0 + kl;
-          valid = valid && ((__ldg(a.mask + (bit >> 5)) >> (bit & 31)) & 1u);
-        }
-        vld[s] = valid;
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float cm = -INFINITY;
-#pragma unroll
-        for (int s = 0; s < STEPS; ++s) cm = vld[s] ? fmaxf(cm, sc[s][g]) : cm;
-#pragma unroll
-        for (int off = LPK; off < 32; off <<= 1) // the warp's key groups
-          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-        if (cm > m[g] + kLazyThreshold || (m[g] == -INFINITY && cm != -INFINITY)) {
-          const float alpha = ex2(m[g] - cm); // 0 when m == -inf
-          l[g] *= alpha;
-          const uint64_t a2 = f32x2(alpha, alpha);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
-          m[g] = cm;
-        }
-      }
-#pragma unroll
-      for (int s = 0; s < STEPS; ++s) {
-        const int kl = s * KPW + grp;
-        const uint4 vw = lds128(sV(st) + kl * L::kRow + sub * 16);
-        const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
-                                bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float p = vld[s] ? ex2(sc[s][g] - m[g]) : 0.f;
-          l[g] += p;
-          const uint64_t p2 = f32x2(p, p);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
-        }
-      }
     } else {
-      // many heads per lane: one rescale decision per key
+      // as above with every lane holding all G scores: SUB steps' scores, one
+      // rescale decision per head for them, then their P.V
 #pragma unroll
-      for (int s = 0; s < STEPS; ++s) {
-        const int kl = s * KPW + grp; // row of the chunk
-        const uint4 kw = lds128(sK(st) + kl * L::kRow + sub * 16);
-        const uint4 vw = lds128(sV(st) + kl * L::kRow + sub * 16);
-        const uint64_t k2[4] = {bf16x2_to_f32x2(kw.x), bf16x2_to_f32x2(kw.y),
-                                bf16x2_to_f32x2(kw.z), bf16x2_to_f32x2(kw.w)};
-        float sc[G];
+      for (int s0 = 0; s0 < STEPS; s0 += SUB) {
+        float sc[SUB][G];
+        bool vld[SUB];
+#pragma unroll
+        for (int s = 0; s < SUB; ++s) {
+          const int kl = (s0 + s) * KPW + grp; // row of the chunk
+          const uint4 kw = lds128(sK(st) + kl * L::kRow + sub * 16);
+          const uint64_t k2[4] = {bf16x2_to_f32x2(kw.x), bf16x2_to_f32x2(kw.y),
+                                  bf16x2_to_f32x2(kw.z), bf16x2_to_f32x2(kw.w)};
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            uint64_t acc = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ffma2(acc, q2[g][k], k2[k]);
+            float x, y;
+            f32x2_split(acc, x, y);
+            sc[s][g] = x + y;
+          }
+          group_reduce<G, LPK>(sc[s]);
+          bool valid = key0 + kl < key_end; // past the split's last key: no weight
+          if constexpr (MASK) {
+            const int64_t bit = mask_row + key0 + kl;
+            valid = valid && ((__ldg(a.mask + (bit >> 5)) >> (bit & 31)) & 1u);
+          }
+          vld[s] = valid;
+        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          uint64_t acc = 0;
+          float cm = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) ffma2(acc, q2[g][k], k2[k]);
-          float x, y;
-          f32x2_split(acc, x, y);
-          sc[g] = x + y;
-        }
-        bool valid = key0 + kl < key_end; // past the split's last key: no weight
-        if constexpr (MASK) {
-          const int64_t bit = mask_row + key0 + kl;
-          valid = valid && ((__ldg(a.mask + (bit >> 5)) >> (bit & 31)) & 1u);
-        }
-        const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
-                                bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
-        group_reduce<G, LPK>(sc);
-        // online softmax with lazy rescale: the running max moves only when a
-        // score exceeds it by more than 2^8 (a function of this lane group's
-        // own keys, so the result is the same in any batch)
+          for (int s = 0; s < SUB; ++s) cm = vld[s] ? fmaxf(cm, sc[s][g]) : cm;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          if (valid && (sc[g] > m[g] + kLazyThreshold || m[g] == -INFINITY)) {
-            const float alpha = ex2(m[g] - sc[g]);
+          for (int off = LPK; off < 32; off <<= 1) // the warp's key groups
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+          if (cm > m[g] + kLazyThreshold || (m[g] == -INFINITY && cm != -INFINITY)) {
+            const float alpha = ex2(m[g] - cm); // 0 when m == -inf
             l[g] *= alpha;
             const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
             for (int k = 0; k < 4; ++k) o2[g][k] = fmul2(o2[g][k], a2);
-            m[g] = sc[g];
+            m[g] = cm;
           }
-          const float p = valid ? ex2(sc[g] - m[g]) : 0.f;
-          l[g] += p;
-          const uint64_t p2 = f32x2(p, p);
+        }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
+        for (int s = 0; s < SUB; ++s) {
+          const int kl = (s0 + s) * KPW + grp;
+          const uint4 vw = lds128(sV(st) + kl * L::kRow + sub * 16);
+          const uint64_t v2[4] = {bf16x2_to_f32x2(vw.x), bf16x2_to_f32x2(vw.y),
+                                  bf16x2_to_f32x2(vw.z), bf16x2_to_f32x2(vw.w)};
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float p = vld[s] ? ex2(sc[s][g] - m[g]) : 0.f;
+            l[g] += p;
+            const uint64_t p2 = f32x2(p, p);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ffma2(o2[g][k], p2, v2[k]);
+          }
         }
       }
     }
