@@ -94,17 +94,18 @@ __device__ __forceinline__ void group_reduce(float (&s)[G]) {
   }
 }
 
-// G == 4, 16 lanes per key: sums the four partial scores over the key's 16
-// lanes and leaves head (sub >> 2)'s total on lanes 4h..4h+3 of the group
-// (identical bits on the four).
+// G == 4, 16 lanes per key: a lane with sub bits b3, b2 holds its four
+// partial scores in the order of heads 2b3+b2, 2b3+!b2, 2!b3+b2, 2!b3+!b2
+// (own_head_order); sums them over the key's 16 lanes and leaves head
+// (sub >> 2)'s total on lanes 4h..4h+3 of the group (identical bits on the
+// four).  The per-lane head order makes every exchange select-free.
+__device__ __forceinline__ int own_head_order(int j, int sub) {
+  return 2 * ((j >> 1) ^ ((sub >> 3) & 1)) + ((j & 1) ^ ((sub >> 2) & 1));
+}
 __device__ __forceinline__ float reduce_scatter4(const float (&s)[4]) {
-  const int sub = threadIdx.x & 15;
-  const bool b3 = (sub >> 3) & 1, b2 = (sub >> 2) & 1;
-  const float kx = b3 ? s[2] : s[0], ky = b3 ? s[3] : s[1];
-  const float sx = b3 ? s[0] : s[2], sy = b3 ? s[1] : s[3];
-  const float px = kx + __shfl_xor_sync(0xffffffffu, sx, 8);
-  const float py = ky + __shfl_xor_sync(0xffffffffu, sy, 8);
-  float c = (b2 ? py : px) + __shfl_xor_sync(0xffffffffu, b2 ? px : py, 4);
+  const float px = s[0] + __shfl_xor_sync(0xffffffffu, s[2], 8);
+  const float py = s[1] + __shfl_xor_sync(0xffffffffu, s[3], 8);
+  float c = px + __shfl_xor_sync(0xffffffffu, py, 4);
   c += __shfl_xor_sync(0xffffffffu, c, 2);
   c += __shfl_xor_sync(0xffffffffu, c, 1);
   return c;
@@ -210,11 +211,13 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
   for (int i = 0; i < NS && i < my_chunks; ++i) issue(i);
 
   // ---- queries of the group as fp32 pairs, pre-scaled by sm_scale * log2(e)
+  // (G == 4 with 16 lanes a key: slot g holds head own_head_order(g, sub))
   uint64_t q2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
+    const int hq = kOwnHead ? own_head_order(g, sub) : g;
     const uint4 w = sub * 8 < Dr ? *reinterpret_cast<const uint4 *>(
-        a.q + (q_row * a.Hq + kvh * G + g) * Dr + sub * 8)
+        a.q + (q_row * a.Hq + kvh * G + hq) * Dr + sub * 8)
                                  : make_uint4(0u, 0u, 0u, 0u);
     const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2);
     q2[g][0] = fmul2(bf16x2_to_f32x2(w.x), sc2);
