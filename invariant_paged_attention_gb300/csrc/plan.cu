@@ -37,22 +37,34 @@ __device__ inline void request_geometry(const PlanArgs &a, int b, int32_t &q_sta
 }
 
 // Exclusive scan of one value per thread across the block; returns the
-// thread's exclusive prefix and writes the block total to *total.
+// thread's exclusive prefix and writes the block total to *total.  Two
+// levels: a shuffle scan inside each warp, then a scan of the 32 warp totals
+// by warp 0 (three block barriers instead of two per doubling step).
 template <typename T>
 __device__ T block_exclusive_scan(T v, T *scratch, T *total) {
-  const int tid = threadIdx.x;
-  scratch[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const T x = tid >= off ? scratch[tid - off] : T(0);
-    __syncthreads();
-    scratch[tid] += x;
-    __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  T incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const T x = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += x;
   }
-  const T incl = scratch[tid];
-  *total = scratch[kPlanThreads - 1];
+  if (lane == 31) scratch[warp] = incl; // warp totals
   __syncthreads();
-  return incl - v;
+  if (warp == 0) {
+    T w = scratch[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const T x = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += x;
+    }
+    scratch[lane] = w; // inclusive prefix of the warp totals
+  }
+  __syncthreads();
+  const T before = warp > 0 ? scratch[warp - 1] : T(0);
+  *total = scratch[kPlanThreads / 32 - 1];
+  __syncthreads(); // scratch is reused by the next scan
+  return before + incl - v;
 }
 
 __device__ inline int find_group_owner(const int32_t *group_off, int batch, int32_t g) {
@@ -68,7 +80,7 @@ __device__ inline int find_group_owner(const int32_t *group_off, int batch, int3
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
-  __shared__ int64_t s_scan[kPlanThreads];
+  __shared__ int64_t s_scan[kPlanThreads / 32];
   __shared__ int s_ok;
   const int tid = threadIdx.x;
   const int32_t gt = group_tiles(a.tiles_per_unit, a.ctas);
