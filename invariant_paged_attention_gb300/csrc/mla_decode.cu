@@ -17,10 +17,11 @@
 //   S^T = C Q^T     M=128 keys, N=16 heads, K=512+64: A = the latent rows
 //                   (K-major, 64-column SW128 pieces), B = the 16 heads'
 //                   q_nope / q_pe (K-major), fp32 accumulator in TMEM
-//   softmax         thread t = key t of the block (TMEM lane t) reads its 16
-//                   heads' scores; per-head block max = redux over the warp,
-//                   then over the 4 warps through shared memory (the same
-//                   value on every thread); lazy online softmax (the running
+//   softmax         thread t of a warpgroup = key t of the block (TMEM lane
+//                   t) reads its group's 8 heads' scores; per-head block max =
+//                   redux over the warp, then over the group's 4 warps through
+//                   shared memory (the same value on every thread of the
+//                   group); lazy online softmax (the running
 //                   max moves only when the block max exceeds it by more than
 //                   2^8; O is then rescaled in TMEM); P = 2^(s - m) as bf16
 //                   into shared memory, row t = key t (MN-major operand)
@@ -32,8 +33,9 @@
 // o = O^T / l and lse (bf16 rows for a request with one split, else fp32
 // partials).
 //
-// Warp roles (9 warps): 0-3 softmax + epilogue, 4 owns TMEM and issues every
-// MMA from one thread, 5-8 copy: one thread loads the 16 heads' q (2-D TMA
+// Warp roles (13 warps): 0-7 softmax + epilogue (two warpgroups of 8 heads
+// each, a thread per key), 8 owns TMEM and issues every MMA from one thread,
+// 9-12 copy: one thread loads the 16 heads' q (2-D TMA
 // boxes), and the 128 threads copy the paged latent rows with 16-byte cp.async
 // straight into the swizzled operand layout (keys past the split or on a bad
 // page are zero-filled; each thread's copies of a ring slot end with an
@@ -66,9 +68,10 @@ constexpr int kKeys = 128;                   // keys per block: the MMA's M
 constexpr int kPiece = kKeys * 128;          // 128 rows x 64 bf16, SW128
 constexpr int kCkvPieces = kMlaCkvDim / 64;  // 8
 constexpr int kPairs = 5;                    // ring slots of two ckv pieces
-constexpr int kThreadsT = 288;
-constexpr int kMmaWarpT = 4;
-constexpr int kProdWarpT = 5;      // warps 5-8 copy the latent rows
+constexpr int kHs = 8;             // heads per softmax warpgroup (two warpgroups)
+constexpr int kThreadsT = 416;
+constexpr int kMmaWarpT = 8;
+constexpr int kProdWarpT = 9;      // warps 9-12 copy the latent rows
 constexpr float kLazyT = 8.0f; // log2 units
 
 struct MlaSmem {
@@ -81,8 +84,8 @@ struct MlaSmem {
   static constexpr int bQFull = 0, bPairFull = 1, bPairEmpty = 1 + kPairs,
                        bKpeFull = 1 + 2 * kPairs, bKpeEmpty = bKpeFull + 1, bSFull = bKpeEmpty + 1,
                        bPFull = bSFull + 1, bPVDone = bPFull + 1, kNumBars = bPVDone + 1;
-  static constexpr int kRed = kBar + 256;              // float [2][4 warps][16 heads]
-  static constexpr int kLred = kRed + 2 * 4 * kHg * 4; // float [4 warps][16 heads]
+  static constexpr int kRed = kBar + 256;              // float [2][2 groups][4 warps][8 heads]
+  static constexpr int kLred = kRed + 2 * 4 * kHg * 4; // float [2 groups][4 warps][8 heads]
   static constexpr int kSlot = kLred + 4 * kHg * 4;
   static constexpr int kBytes = kSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     mbar_init(bar(L::bKpeFull), 128);
     mbar_init(bar(L::bKpeEmpty), 1);
     mbar_init(bar(L::bSFull), 1);
-    mbar_init(bar(L::bPFull), 4); // one arrival per softmax warp
+    mbar_init(bar(L::bPFull), 8); // one arrival per softmax warp
     mbar_init(bar(L::bPVDone), 1);
     fence_mbar_init();
   }
@@ -295,12 +298,17 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = tid; // key of the block = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // two warpgroups, each owning 8 of the 16 heads; warp w%4 of a group
+    // covers TMEM lanes (keys) 32(w%4)..+31
+    const int gs = warp >> 2, qd = warp & 3;
+    const int t = qd * 32 + lane; // key of the block = TMEM lane
+    const int h0 = gs * kHs;      // first head of this group
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    const uint32_t gbar = 1 + gs; // the group's named barrier
     float *red = reinterpret_cast<float *>(smem + L::kRed);
-    float m[kHg], l[kHg];
+    float m[kHs], l[kHs];
 #pragma unroll
-    for (int h = 0; h < kHg; ++h) {
+    for (int h = 0; h < kHs; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
     }
@@ -311,57 +319,58 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         break;
       }
       tc_fence_after();
-      uint32_t v[kHg];
-      tmem_ld16(tS + lane_base, v);
+      uint32_t v[kHs];
+      tmem_ld8(tS + h0 + lane_base, v);
       tmem_wait_ld();
       const bool valid = key_begin + j * kKeys + t < key_end;
-      float s[kHg];
+      float s[kHs];
 #pragma unroll
-      for (int h = 0; h < kHg; ++h)
-        s[h] = (valid && h < h_real) ? __uint_as_float(v[h]) * a.scale_log2 : -INFINITY;
-      // block max per head: over the warp, then the 4 warps (same value everywhere)
+      for (int h = 0; h < kHs; ++h)
+        s[h] = (valid && h0 + h < h_real) ? __uint_as_float(v[h]) * a.scale_log2 : -INFINITY;
       // P against the running max, computed while the block max is exchanged
       // (the running max rarely moves: then these are the final values)
-      float p[kHg];
+      float p[kHs];
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) {
+      for (int h = 0; h < kHs; ++h) {
         const float ms = m[h] == -INFINITY ? 0.f : m[h];
         p[h] = s[h] == -INFINITY ? 0.f : ex2(s[h] - ms);
       }
-      float *rd = red + (j & 1) * 4 * kHg;
+      // block max per head: over the warp, then the group's 4 warps (the same
+      // value on every thread of the group)
+      float *rd = red + ((j & 1) * 2 + gs) * 4 * kHs;
       float mine = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) {
+      for (int h = 0; h < kHs; ++h) {
         const float wm = warp_max(s[h]);
         mine = lane == h ? wm : mine;
       }
-      if (lane < kHg) rd[warp * kHg + lane] = mine;
-      bar_sync_named(1, 128);
+      if (lane < kHs) rd[qd * kHs + lane] = mine;
+      bar_sync_named(gbar, 128);
       // lazy online softmax: the running max of a head moves only when the
       // block max exceeds it by more than 2^8; such a head's P is recomputed
-      float bmv[kHg];
+      float bmv[kHs];
 #pragma unroll
-      for (int h4 = 0; h4 < kHg / 4; ++h4) {
+      for (int h4 = 0; h4 < kHs / 4; ++h4) {
         const float4 w0 = reinterpret_cast<const float4 *>(rd)[h4];
-        const float4 w1 = reinterpret_cast<const float4 *>(rd + kHg)[h4];
-        const float4 w2 = reinterpret_cast<const float4 *>(rd + 2 * kHg)[h4];
-        const float4 w3 = reinterpret_cast<const float4 *>(rd + 3 * kHg)[h4];
+        const float4 w1 = reinterpret_cast<const float4 *>(rd + kHs)[h4];
+        const float4 w2 = reinterpret_cast<const float4 *>(rd + 2 * kHs)[h4];
+        const float4 w3 = reinterpret_cast<const float4 *>(rd + 3 * kHs)[h4];
         bmv[4 * h4 + 0] = fmaxf(fmaxf(w0.x, w1.x), fmaxf(w2.x, w3.x));
         bmv[4 * h4 + 1] = fmaxf(fmaxf(w0.y, w1.y), fmaxf(w2.y, w3.y));
         bmv[4 * h4 + 2] = fmaxf(fmaxf(w0.z, w1.z), fmaxf(w2.z, w3.z));
         bmv[4 * h4 + 3] = fmaxf(fmaxf(w0.w, w1.w), fmaxf(w2.w, w3.w));
       }
-      uint32_t up = 0; // heads whose running max moves (the same on every thread)
+      uint32_t up = 0; // heads whose running max moves (the same on the group)
 #pragma unroll
-      for (int h = 0; h < kHg; ++h)
+      for (int h = 0; h < kHs; ++h)
         if (bmv[h] > m[h] + kLazyT || (m[h] == -INFINITY && bmv[h] != -INFINITY)) up |= 1u << h;
-      float alpha[kHg];
+      float alpha[kHs];
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) alpha[h] = 1.f;
+      for (int h = 0; h < kHs; ++h) alpha[h] = 1.f;
       const bool resc = up != 0;
       if (resc) {
 #pragma unroll
-        for (int h = 0; h < kHg; ++h) {
+        for (int h = 0; h < kHs; ++h) {
           if ((up >> h) & 1u) {
             alpha[h] = ex2(m[h] - bmv[h]); // 0 when m == -inf
             m[h] = bmv[h];
@@ -370,31 +379,29 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         }
       }
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) l[h] = fmaf(l[h], alpha[h], p[h]);
+      for (int h = 0; h < kHs; ++h) l[h] = fmaf(l[h], alpha[h], p[h]);
       // the previous P.V is done: P's buffer is free and O may be rescaled
       if (j > 0 && !mbar_wait(bar(L::bPVDone), (j - 1) & 1, a.status)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      if (j > 0 && resc) { // resc is the same on every thread
+      if (j > 0 && resc) { // resc is the same on the group
 #pragma unroll
         for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
-          uint32_t o[kHg];
-          tmem_ld16(tO(mb) + lane_base, o);
+          uint32_t o[kHs];
+          tmem_ld8(tO(mb) + h0 + lane_base, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < kHg; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-          tmem_st16(tO(mb) + lane_base, o);
+          for (int h = 0; h < kHs; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+          tmem_st8(tO(mb) + h0 + lane_base, o);
         }
         tmem_wait_st();
       }
-      // P row of key t: heads 0-7 in 16-byte chunk 0, heads 8-15 in chunk 1
-      const uint32_t prow = sbase + L::kP;
-      sts128(prow + sw128(t, 0), make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
-                                            pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7])));
-      sts128(prow + sw128(t, 1), make_uint4(pack_bf16(p[8], p[9]), pack_bf16(p[10], p[11]),
-                                            pack_bf16(p[12], p[13]), pack_bf16(p[14], p[15])));
+      // P row of key t: this group's 8 heads are 16-byte chunk gs of the row
+      sts128(sbase + L::kP + sw128(t, gs),
+             make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
+                        pack_bf16(p[6], p[7])));
       fence_proxy_async(); // P is read by the MMA (async proxy)
       tc_fence_before();
       __syncwarp();
@@ -402,47 +409,47 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     }
 
     // ---- epilogue: l = sum of every thread's partial sums (warp butterfly,
-    // then the 4 warps in order), o = O^T / l, lse = (m + log2 l) ln 2
+    // then the group's 4 warps in order), o = O^T / l, lse = (m + log2 l) ln 2
     const bool have = __all_sync(0xffffffffu, !failed && nb > 0 &&
                                                   mbar_wait(bar(L::bPVDone), (nb - 1) & 1,
                                                             a.status));
     tc_fence_after();
 #pragma unroll
-    for (int h = 0; h < kHg; ++h)
+    for (int h = 0; h < kHs; ++h)
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
-    float *lr = reinterpret_cast<float *>(smem + L::kLred);
+    float *lr = reinterpret_cast<float *>(smem + L::kLred) + gs * 4 * kHs;
     float lw = 0.f;
 #pragma unroll
-    for (int h = 0; h < kHg; ++h) lw = lane == h ? l[h] : lw;
-    if (lane < kHg) lr[warp * kHg + lane] = lw;
-    bar_sync_named(1, 128);
-    float inv[kHg];
-    bool nz[kHg];
+    for (int h = 0; h < kHs; ++h) lw = lane == h ? l[h] : lw;
+    if (lane < kHs) lr[qd * kHs + lane] = lw;
+    bar_sync_named(gbar, 128);
+    float inv[kHs];
+    bool nz[kHs];
     float lse_mine = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < kHg; ++h) {
-      const float ls = __fadd_rn(__fadd_rn(__fadd_rn(lr[h], lr[kHg + h]), lr[2 * kHg + h]),
-                                 lr[3 * kHg + h]);
+    for (int h = 0; h < kHs; ++h) {
+      const float ls = __fadd_rn(__fadd_rn(__fadd_rn(lr[h], lr[kHs + h]), lr[2 * kHs + h]),
+                                 lr[3 * kHs + h]);
       nz[h] = have && ls > 0.f;
       inv[h] = nz[h] ? __frcp_rn(ls) : 0.f;
       const float lse = nz[h] ? __fmul_rn(__fadd_rn(m[h], lg2(ls)), kLn2) : -INFINITY;
       lse_mine = t == h ? lse : lse_mine;
     }
     const bool single = (r.kv_len - 1) / a.split == 0; // one split: the final row
-    const int64_t head0 = static_cast<int64_t>(r.q_start) * a.Hq + hg * kHg;
-    const int64_t prow0 = (r.rowbase + u.split) * a.Hq + hg * kHg;
+    const int64_t head0 = static_cast<int64_t>(r.q_start) * a.Hq + hg * kHg + h0;
+    const int64_t prow0 = (r.rowbase + u.split) * a.Hq + hg * kHg + h0;
 #pragma unroll
     for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
-      uint32_t o[kHg];
+      uint32_t o[kHs];
       if (have) {
-        tmem_ld16(tO(mb) + lane_base, o);
+        tmem_ld8(tO(mb) + h0 + lane_base, o);
         tmem_wait_ld();
       }
       const int d = mb * 128 + t; // latent column of this thread
 #pragma unroll
-      for (int h = 0; h < kHg; ++h) {
-        if (h >= h_real) break;
+      for (int h = 0; h < kHs; ++h) {
+        if (h0 + h >= h_real) break;
         const float val = nz[h] ? __fmul_rn(__uint_as_float(o[h]), inv[h]) : 0.f;
         if (single)
           a.out[(head0 + h) * kMlaCkvDim + d] = to_bf16(val);
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           a.part_o[(prow0 + h) * kMlaCkvDim + d] = val;
       }
     }
-    if (t < h_real) {
+    if (t < kHs && h0 + t < h_real) {
       if (single) {
         if (a.lse) a.lse[head0 + t] = lse_mine;
       } else {
