@@ -27,9 +27,6 @@ __device__ __forceinline__ float lg2(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 // Round-to-nearest-even fp32 -> bf16 pair, first element in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
@@ -163,18 +160,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
-// TMA gather of four rows (y0..y3) x one 64-column box at column x of a 2-D
-// tensor map into shared memory (four consecutive 128-byte rows, swizzled as
-// the map says); completes 4 * box bytes on `bar`.  Rows outside the map read
-// as zeros.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar) {
-  asm volatile("cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx"
-               "::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-               "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-               : "memory");
-}
-
 // A 2-D tiled TMA load (column x, row y) into this CTA's shared memory,
 // completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y,
@@ -195,9 +180,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int3
                : "memory");
 }
 
-// The same gather, written at the same shared-memory offset of every CTA of
-// the cluster in cta_mask; each destination CTA's barrier at offset `bar`
-// receives the complete_tx of the bytes written into that CTA.
+// TMA gather of four rows (y0..y3) x one 64-column box at column x of a 2-D
+// tensor map (four consecutive 128-byte rows, swizzled as the map says; rows
+// outside the map read as zeros), written at the same shared-memory offset of
+// every CTA of the cluster in cta_mask; each destination CTA's barrier at
+// offset `bar` receives the complete_tx of the bytes written into that CTA.
 __device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const void *tmap, int32_t x,
                                                int32_t y0, int32_t y1, int32_t y2, int32_t y3,
                                                uint32_t bar, uint16_t cta_mask) {
@@ -232,15 +219,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
                "r"(valid ? 16 : 0)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tcgen05.mma operand reads).
@@ -317,18 +297,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
       : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 
