@@ -61,52 +61,50 @@ __device__ __forceinline__ int owner(const int32_t *qo_indptr, int batch, int64_
 }
 
 // Merge of the split partials a prefill / decode call left in the workspace:
-// CTAs stride over the q tokens (most tokens of a long prefill need no merge,
-// and skipping them in a loop is cheaper than launching a CTA each), a
-// token's q heads spread over the warps.  A warp folds one row: lane s first
-// loads the LSE of split s (all splits in flight at once), then the states
-// are folded in ascending split order.  Rows whose q tile had a single split
-// were written by the attention kernel and are skipped.
+// one CTA per q token, its q heads spread over the warps.  A warp folds one
+// row: lane s first loads the LSE of split s (all splits in flight at once),
+// then the states are folded in ascending split order.  Rows whose q tile had
+// a single split were written by the attention kernel and are skipped.
 template <int V>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_partials_kernel(const AttnArgs a) {
   const int D = a.D;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int64_t token = blockIdx.x; token < a.total_rows; token += gridDim.x) {
-    const int b = a.qo_indptr ? owner(a.qo_indptr, a.batch, token) : static_cast<int>(token);
-    const ReqInfo r = a.reqs[b];
-    const int32_t t = static_cast<int32_t>(token - r.q_start);
-    const int32_t tile = t / a.tile_tokens;
-    const int32_t n_tile = tile_splits(r.q_len, r.kv_len, tile, a.tile_tokens, a.causal, a.split);
-    if (n_tile <= 1 || r.rowbase < 0) continue;
-    const int32_t p = a.causal ? r.kv_len - r.q_len + t : r.kv_len - 1;
-    const int32_t n_row = min(n_tile, p / a.split + 1);
-    const int64_t base = (r.rowbase + static_cast<int64_t>(t) * r.nsp) * a.Hq;
-    for (int h = warp; h < a.Hq; h += kMergeWarps) {
-      float L = -INFINITY;
-      float o[V];
+  const int64_t token = blockIdx.x;
+  if (token >= a.total_rows) return;
+  const int b = a.qo_indptr ? owner(a.qo_indptr, a.batch, token) : static_cast<int>(token);
+  const ReqInfo r = a.reqs[b];
+  const int32_t t = static_cast<int32_t>(token - r.q_start);
+  const int32_t tile = t / a.tile_tokens;
+  const int32_t n_tile = tile_splits(r.q_len, r.kv_len, tile, a.tile_tokens, a.causal, a.split);
+  if (n_tile <= 1 || r.rowbase < 0) return;
+  const int32_t p = a.causal ? r.kv_len - r.q_len + t : r.kv_len - 1;
+  const int32_t n_row = min(n_tile, p / a.split + 1);
+  const int64_t base = (r.rowbase + static_cast<int64_t>(t) * r.nsp) * a.Hq;
+  for (int h = warp; h < a.Hq; h += kMergeWarps) {
+    float L = -INFINITY;
+    float o[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) o[i] = 0.f;
+    for (int s0 = 0; s0 < n_row; s0 += 32) {
+      const int n_here = min(32, n_row - s0);
+      const float ls_lane = lane < n_here
+          ? __ldg(a.part_lse + base + static_cast<int64_t>(s0 + lane) * a.Hq + h) : -INFINITY;
+      for (int k = 0; k < n_here; ++k) {
+        const float ls = __shfl_sync(0xffffffffu, ls_lane, k);
+        if (ls == -INFINITY) continue;
+        const int64_t idx = base + static_cast<int64_t>(s0 + k) * a.Hq + h;
+        float v[V];
+        load_state<V>(a.part_o + idx * D, D, lane, v);
+        fold_state<V>(L, o, ls, v);
+      }
+    }
+    if (L == -INFINITY) {
 #pragma unroll
       for (int i = 0; i < V; ++i) o[i] = 0.f;
-      for (int s0 = 0; s0 < n_row; s0 += 32) {
-        const int n_here = min(32, n_row - s0);
-        const float ls_lane = lane < n_here
-            ? __ldg(a.part_lse + base + static_cast<int64_t>(s0 + lane) * a.Hq + h) : -INFINITY;
-        for (int k = 0; k < n_here; ++k) {
-          const float ls = __shfl_sync(0xffffffffu, ls_lane, k);
-          if (ls == -INFINITY) continue;
-          const int64_t idx = base + static_cast<int64_t>(s0 + k) * a.Hq + h;
-          float v[V];
-          load_state<V>(a.part_o + idx * D, D, lane, v);
-          fold_state<V>(L, o, ls, v);
-        }
-      }
-      if (L == -INFINITY) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) o[i] = 0.f;
-      }
-      const int64_t row = token * a.Hq + h;
-      store_row<V>(a.out + row * D, D, a.lse ? a.lse + row : nullptr, lane, L, o);
     }
+    const int64_t row = token * a.Hq + h;
+    store_row<V>(a.out + row * D, D, a.lse ? a.lse + row : nullptr, lane, L, o);
   }
 }
 
@@ -146,8 +144,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t st) {
   if (a.total_rows == 0) return cudaSuccess;
-  // a few CTAs per SM of a GB300-sized part, striding over the tokens
-  const unsigned grid = static_cast<unsigned>(a.total_rows < 1216 ? a.total_rows : 1216);
+  const unsigned grid = static_cast<unsigned>(a.total_rows);
   if (a.D <= 128)
     merge_partials_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(a);
   else if (a.D <= 256) // head_dim 256: eight floats per lane
