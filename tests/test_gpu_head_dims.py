@@ -95,3 +95,15 @@ def test_d256_chunked_prefill_and_batch_invariance():
     so, sl = run_prefill(solo)
     a, b = int(whole.qo_indptr[1]), int(whole.qo_indptr[2])
     assert same_bits(so, ref_o[a:b]) and same_bits(sl, ref_l[a:b])
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (8, 8), (32, 16)])
+def test_decode_d256_other_group_sizes(Hq, Hkv):
+    """Group sizes 8, 1 and 2 at head_dim 256 (a chunk's lazy-rescale decision
+    is taken per 2-step sub-chunk at G=8, per chunk otherwise)."""
+    store = wl.PagedStore([wl.Sequence(2200 + i, c - 1, 1) for i, c in
+                           enumerate([1, 3000, 4097, 200])], Hq, Hkv, 256, 16, DEV,
+                          layout_seed=34)
+    call = wl.whole_prefill(store)
+    out, lse = run_decode(call)
+    check_rows(call, out, lse)
