@@ -13,8 +13,9 @@
  * it occupies, the number of SMs or the launch grid, or where a chunk
  * boundary falls ("sglang PR #43612", Summary: chunked prefill must
  * reproduce the unchunked one when chunks start on the 128-row q-tile grid,
- * 128 / gqa_group tokens; this library also reproduces it off that grid, but
- * callers may only rely on the grid).
+ * 128 / gqa_group tokens; this library also reproduces it off that grid
+ * unless an off-grid chunk leaves a q tile holding a single token, which is
+ * computed by the streaming path; callers may only rely on the grid).
  *
  * Layouts (all row-major, all device pointers unless named *_host):
  *   q        [total_q, num_qo_heads, head_dim] bf16 (decode: [batch, ...])
