@@ -123,6 +123,63 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+BF16, F32, I32, I64, U8 = torch.bfloat16, torch.float32, torch.int32, torch.int64, torch.uint8
+
+
+# The library sees only the addresses of the device tensors: a host tensor, a
+# strided view or a tensor of another dtype would be read as a dense device
+# array of the stated type.  So every call checks its tensors first: dtype and
+# layout (_check_types), the shapes the sizes it passes are taken from, and
+# last that all of them live on one CUDA device (_check_cuda).
+
+
+def _check_types(*specs):
+    """Each spec is (name, tensor, dtype[, optional]): dtype None takes any
+    dtype (a byte buffer); an optional argument may be None.  Returns the
+    (name, tensor) pairs that were given."""
+    given = []
+    for spec in specs:
+        name, t, dtype = spec[:3]
+        if t is None:
+            if len(spec) > 3 and spec[3]:
+                continue
+            raise TypeError(f"{name} is required")
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        given.append((name, t))
+    return given
+
+
+def _check_cuda(given):
+    device = None
+    for name, t in given:
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the other arguments on {device}")
+
+
+def _check_rows(q, out, lse, qname="q"):
+    """out has q's shape; lse, when given, one float per (token, head) of q."""
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out has shape {tuple(out.shape)}, {qname} {tuple(q.shape)}")
+    if lse is not None and (q.dim() < 2 or lse.numel() != q.shape[0] * q.shape[1]):
+        raise ValueError(f"lse must hold {qname}.shape[0] x {qname}.shape[1] floats")
+
+
+def _check_caches(k_cache, v_cache):
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.dim() != 4:
+        raise ValueError(f"k_cache and v_cache must both be [num_pages, page_size, "
+                         f"num_kv_heads, head_dim], got {tuple(k_cache.shape)} and "
+                         f"{tuple(v_cache.shape)}")
+
+
 def _host_i32(t) -> torch.Tensor:
     t = torch.as_tensor(t, dtype=torch.int32)
     if t.device.type != "cpu":
@@ -166,6 +223,13 @@ def bia_decode_workspace_size(desc, kv_indptr_host, kv_last_page_len_host, split
 def bia_prefill_paged(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices,
                       kv_last_page_len, qo_indptr_host, kv_indptr_host, kv_last_page_len_host,
                       workspace, out, lse=None, causal=True, split_size=0, stream=None):
+    ts = _check_types(("q", q, BF16), ("k_cache", k_cache, BF16), ("v_cache", v_cache, BF16),
+                      ("qo_indptr", qo_indptr, I32), ("kv_indptr", kv_indptr, I32),
+                      ("kv_indices", kv_indices, I32), ("kv_last_page_len", kv_last_page_len, I32),
+                      ("workspace", workspace, None), ("out", out, BF16), ("lse", lse, F32, True))
+    _check_caches(k_cache, v_cache)
+    _check_rows(q, out, lse)
+    _check_cuda(ts)
     qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
                      _host_i32(kv_last_page_len_host))
     rc = load().bia_prefill_paged(
@@ -184,6 +248,14 @@ def bia_prefill_paged_mask(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_i
     """bia_prefill_paged with a custom mask: ``mask`` a device uint8 tensor of
     little-endian bits, ``mask_indptr`` its device int64 [batch+1] bit
     offsets (include/bia.h states the rule)."""
+    ts = _check_types(("q", q, BF16), ("k_cache", k_cache, BF16), ("v_cache", v_cache, BF16),
+                      ("qo_indptr", qo_indptr, I32), ("kv_indptr", kv_indptr, I32),
+                      ("kv_indices", kv_indices, I32), ("kv_last_page_len", kv_last_page_len, I32),
+                      ("mask", mask, U8), ("mask_indptr", mask_indptr, I64),
+                      ("workspace", workspace, None), ("out", out, BF16), ("lse", lse, F32, True))
+    _check_caches(k_cache, v_cache)
+    _check_rows(q, out, lse)
+    _check_cuda(ts)
     qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
                      _host_i32(kv_last_page_len_host))
     mih = torch.as_tensor(mask_indptr_host, dtype=torch.int64).contiguous()
@@ -202,6 +274,13 @@ def bia_prefill_paged_mask(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_i
 def bia_decode_paged(desc, q, k_cache, v_cache, kv_indptr, kv_indices, kv_last_page_len,
                      kv_indptr_host, kv_last_page_len_host, workspace, out, lse=None,
                      split_size=0, stream=None):
+    ts = _check_types(("q", q, BF16), ("k_cache", k_cache, BF16), ("v_cache", v_cache, BF16),
+                      ("kv_indptr", kv_indptr, I32), ("kv_indices", kv_indices, I32),
+                      ("kv_last_page_len", kv_last_page_len, I32), ("workspace", workspace, None),
+                      ("out", out, BF16), ("lse", lse, F32, True))
+    _check_caches(k_cache, v_cache)
+    _check_rows(q, out, lse)
+    _check_cuda(ts)
     kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
     rc = load().bia_decode_paged(
         ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -221,6 +300,13 @@ def bia_decode_paged_noalloc(desc, q, k_cache, v_cache, kv_indptr, kv_indices, k
     """bia_decode_paged for callers that cannot allocate device memory: no
     workspace argument; the library's static scratch array is used instead
     (see include/bia.h for its size, first-call and concurrency rules)."""
+    ts = _check_types(("q", q, BF16), ("k_cache", k_cache, BF16), ("v_cache", v_cache, BF16),
+                      ("kv_indptr", kv_indptr, I32), ("kv_indices", kv_indices, I32),
+                      ("kv_last_page_len", kv_last_page_len, I32), ("out", out, BF16),
+                      ("lse", lse, F32, True))
+    _check_caches(k_cache, v_cache)
+    _check_rows(q, out, lse)
+    _check_cuda(ts)
     kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
     rc = load().bia_decode_paged_noalloc(
         ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -236,6 +322,14 @@ def bia_append_paged_kv(desc, k_new, v_new, k_cache, v_cache, append_indptr, kv_
     """Write the new tokens' K/V rows [total_new, Hkv, D] into the last
     n_new positions of each request's pages (include/bia.h states the rule);
     `status` is an optional 1-element device int32 tensor."""
+    ts = _check_types(("k_new", k_new, BF16), ("v_new", v_new, BF16), ("k_cache", k_cache, BF16),
+                      ("v_cache", v_cache, BF16), ("append_indptr", append_indptr, I32),
+                      ("kv_indptr", kv_indptr, I32), ("kv_indices", kv_indices, I32),
+                      ("kv_last_page_len", kv_last_page_len, I32), ("status", status, I32, True))
+    _check_caches(k_cache, v_cache)
+    if tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError(f"v_new has shape {tuple(v_new.shape)}, k_new {tuple(k_new.shape)}")
+    _check_cuda(ts)
     ap, kvp, last = (_host_i32(append_indptr_host), _host_i32(kv_indptr_host),
                      _host_i32(kv_last_page_len_host))
     rc = load().bia_append_paged_kv(
@@ -249,7 +343,19 @@ def bia_append_paged_kv(desc, k_new, v_new, k_cache, v_cache, append_indptr, kv_
 
 def bia_merge_states(v, s, out, out_lse=None, num_states=None, stream=None):
     """v [n, S, H, D] fp32, s [n, S, H] fp32 -> out [n, H, D] bf16, out_lse [n, H]."""
+    ts = _check_types(("v", v, F32), ("s", s, F32), ("out", out, BF16),
+                      ("out_lse", out_lse, F32, True), ("num_states", num_states, I32, True))
+    if v.dim() != 4:
+        raise ValueError(f"v must be [n, S, H, D], got shape {tuple(v.shape)}")
     n, S, H, D = v.shape
+    if tuple(s.shape) != (n, S, H) or tuple(out.shape) != (n, H, D):
+        raise ValueError(f"s must be {(n, S, H)} and out {(n, H, D)}, got "
+                         f"{tuple(s.shape)} and {tuple(out.shape)}")
+    if out_lse is not None and tuple(out_lse.shape) != (n, H):
+        raise ValueError(f"out_lse must be {(n, H)}, got {tuple(out_lse.shape)}")
+    if num_states is not None and num_states.numel() != n:
+        raise ValueError(f"num_states must hold {n} counts, got {num_states.numel()}")
+    _check_cuda(ts)
     rc = load().bia_merge_states(_ptr(v), _ptr(s), _ptr(num_states), n, S, H, D, _ptr(out),
                                  _ptr(out_lse), _stream(stream))
     if rc != BIA_OK:
@@ -257,6 +363,8 @@ def bia_merge_states(v, s, out, out_lse=None, num_states=None, stream=None):
 
 
 def bia_read_status(workspace, stream=None) -> int:
+    ts = _check_types(("workspace", workspace, None))
+    _check_cuda(ts)
     st = ctypes.c_int32(0)
     rc = load().bia_read_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
     if rc != BIA_OK:
@@ -296,6 +404,14 @@ def bia_mla_decode_paged(desc, q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv
                          kv_last_page_len, kv_indptr_host, kv_last_page_len_host, workspace,
                          out, lse=None, split_size=0, stream=None):
     """Multi-head latent attention decode (include/bia.h states the layouts)."""
+    ts = _check_types(("q_nope", q_nope, BF16), ("q_pe", q_pe, BF16), ("ckv_cache", ckv_cache, BF16),
+                      ("kpe_cache", kpe_cache, BF16), ("kv_indptr", kv_indptr, I32),
+                      ("kv_indices", kv_indices, I32), ("kv_last_page_len", kv_last_page_len, I32),
+                      ("workspace", workspace, None), ("out", out, BF16), ("lse", lse, F32, True))
+    if kpe_cache.dim() < 1 or ckv_cache.dim() < 1 or kpe_cache.shape[0] != ckv_cache.shape[0]:
+        raise ValueError("ckv_cache and kpe_cache must have the same number of pages")
+    _check_rows(q_nope, out, lse, "q_nope")
+    _check_cuda(ts)
     kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
     rc = load().bia_mla_decode_paged(
         ctypes.byref(desc), _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
