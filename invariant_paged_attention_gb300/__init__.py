@@ -7,7 +7,11 @@ no fallback: if the library is missing or fails to load, every call raises.
 
 The functions carry the C names of ``include/bia.h`` and take torch tensors:
 device tensors for the data and the device copies of the index arrays, CPU
-int32 tensors for the host mirrors.
+int32 tensors for the host mirrors.  Before a call reaches the library, its
+device tensors are checked for dtype, contiguity, the shapes the passed sizes
+come from and one common CUDA device (TypeError / ValueError); everything
+else (descriptor, index arrays, workspace size) is checked by the library
+itself, which raises BiaError with its status code.
 """
 from __future__ import annotations
 

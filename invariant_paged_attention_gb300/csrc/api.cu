@@ -99,19 +99,18 @@ int host_plan(const bia_attn_desc *d, const int32_t *qo, const int32_t *kvp,
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no direct
-// link against the driver library).
+// link against the driver library).  Looked up once; the initialisation of a
+// function-local static is thread-safe, so concurrent first calls agree.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -636,10 +635,11 @@ const char *bia_status_string(int status) {
 int bia_read_status(const void *workspace, int32_t *status_out, void *stream) {
   if (!workspace || !status_out) return BIA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(status_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, st) !=
-      cudaSuccess)
-    return BIA_ERR_CUDA;
-  return cudaStreamSynchronize(st) == cudaSuccess ? BIA_OK : BIA_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(status_out, workspace, sizeof(int32_t),
+                                  cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail("status copy", e);
+  e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? BIA_OK : cuda_fail("status copy synchronize", e);
 }
 
 void bia_set_profile_events(void *attn_begin, void *attn_end) {
