@@ -47,7 +47,12 @@
  * outside [0, num_pages) is caught on the device: the row is read as zeros and
  * bit 0 of the workspace status word is set (bia_read_status).
  *
- * Supported: head_dim 64, 96 or 128 (96 runs zero-padded on the 128 kernels);
+ * Alignment: q, out, the caches and every bf16 row buffer start on a 16-byte
+ * boundary; int32 and fp32 arrays on 4 bytes, int64 arrays on 8; a call
+ * given a pointer off its boundary returns BIA_ERR_INVALID_ARG.
+ *
+ * Supported: head_dim 64, 96, 128 or 256 (96 runs zero-padded on the 128
+ * kernels);
  * num_qo_heads / num_kv_heads in {1,2,4,8};
  * page_size a power of two in 1..256; split sizes positive multiples of 128.
  */

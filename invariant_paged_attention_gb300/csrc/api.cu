@@ -41,6 +41,12 @@ struct HostPlan {
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
+// True when a non-null pointer is not a multiple of `align` bytes (the
+// kernels read int32 / fp32 words, int64 offsets and 16-byte vectors).
+bool misaligned(const void *p, uintptr_t align) {
+  return (reinterpret_cast<uintptr_t>(p) & (align - 1)) != 0;
+}
+
 int log2i(int x) {
   int s = 0;
   while ((1 << s) < x) ++s;
@@ -183,7 +189,7 @@ struct MaskArgs {
 int check_mask(const MaskArgs &m, const int32_t *qo, const int32_t *kvp, const int32_t *last,
                int32_t batch, int page_size) {
   if (!m.bits || !m.indptr || !m.indptr_host) return BIA_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(m.bits) & 3u) return BIA_ERR_INVALID_ARG;
+  if (misaligned(m.bits, 4) || misaligned(m.indptr, 8)) return BIA_ERR_INVALID_ARG;
   const int64_t total_bits = static_cast<int64_t>(m.bytes / 4) * 32;
   for (int b = 0; b < batch; ++b) {
     const int64_t q_len = static_cast<int64_t>(qo[b + 1]) - qo[b];
@@ -208,9 +214,10 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
       !workspace || num_pages <= 0)
     return BIA_ERR_INVALID_ARG;
   if (!decode && (!qo_indptr || !qo_host)) return BIA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BIA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(k_cache) & 15u) ||
-      (reinterpret_cast<uintptr_t>(v_cache) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u))
+  if (misaligned(workspace, 256)) return BIA_ERR_INVALID_ARG;
+  if (misaligned(q, 16) || misaligned(k_cache, 16) || misaligned(v_cache, 16) ||
+      misaligned(out, 16) || misaligned(lse, 4) || misaligned(qo_indptr, 4) ||
+      misaligned(kv_indptr, 4) || misaligned(kv_indices, 4) || misaligned(kv_last_page_len, 4))
     return BIA_ERR_INVALID_ARG;
   if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
   const int G = desc->num_qo_heads / desc->num_kv_heads;
@@ -307,7 +314,10 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   }
 
   const bool profile = g_attn_begin != nullptr && g_attn_end != nullptr;
-  if (profile && cudaEventRecord(g_attn_begin, st) != cudaSuccess) return BIA_ERR_CUDA;
+  if (profile) {
+    const cudaError_t re = cudaEventRecord(g_attn_begin, st);
+    if (re != cudaSuccess) return cuda_fail("profile event record", re);
+  }
   cudaError_t e = decode                     ? bia::launch_decode(a, st)
                   : desc->head_dim == 256 ? bia::launch_prefill_wide(a, st)
                                           : bia::launch_prefill(a, st);
@@ -321,7 +331,10 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
     if (e != cudaSuccess) return cuda_fail("streamed-tile kernel launch", e);
     __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   }
-  if (profile && cudaEventRecord(g_attn_end, st) != cudaSuccess) return BIA_ERR_CUDA;
+  if (profile) {
+    const cudaError_t re = cudaEventRecord(g_attn_end, st);
+    if (re != cudaSuccess) return cuda_fail("profile event record", re);
+  }
   if (hp.part_rows > 0) {
     e = bia::launch_merge_partials(a, st);
     if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
@@ -416,12 +429,13 @@ int bia_merge_states(const float *v, const float *s, const int32_t *num_states, 
   if (head_dim % 4 != 0 || head_dim > 512) return BIA_ERR_UNSUPPORTED;
   if (n == 0) return BIA_OK;
   if (!v || !s || !out) return BIA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(v) & 15u) || (reinterpret_cast<uintptr_t>(out) & 7u))
+  if (misaligned(v, 16) || misaligned(out, 8) || misaligned(s, 4) || misaligned(out_lse, 4) ||
+      misaligned(num_states, 4))
     return BIA_ERR_INVALID_ARG;
   cudaError_t e = bia::launch_merge_states(v, s, num_states, n, num_states_max, num_heads,
                                            head_dim, static_cast<uint16_t *>(out), out_lse,
                                            static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return BIA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
   __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   return BIA_OK;
 }
@@ -449,7 +463,7 @@ int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void
     if (n_new > kv_len) return BIA_ERR_INVALID_ARG;
   }
   const int64_t total_new = append_indptr_host[batch];
-  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return BIA_ERR_INVALID_ARG;
+  if (misaligned(status, 4)) return BIA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (status) {
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
@@ -459,8 +473,9 @@ int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void
   if (!k_new || !v_new || !k_cache || !v_cache || !append_indptr || !kv_indptr || !kv_indices ||
       !kv_last_page_len || num_pages <= 0)
     return BIA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(k_new) & 15u) || (reinterpret_cast<uintptr_t>(v_new) & 15u) ||
-      (reinterpret_cast<uintptr_t>(k_cache) & 15u) || (reinterpret_cast<uintptr_t>(v_cache) & 15u))
+  if (misaligned(k_new, 16) || misaligned(v_new, 16) || misaligned(k_cache, 16) ||
+      misaligned(v_cache, 16) || misaligned(append_indptr, 4) || misaligned(kv_indptr, 4) ||
+      misaligned(kv_indices, 4) || misaligned(kv_last_page_len, 4))
     return BIA_ERR_INVALID_ARG;
   bia::AppendArgs a{};
   a.k_new = static_cast<const uint16_t *>(k_new);
@@ -522,10 +537,10 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
   if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indptr || !kv_indices ||
       !kv_last_page_len || !out || !workspace || num_pages <= 0)
     return BIA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BIA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(q_nope) & 15u) || (reinterpret_cast<uintptr_t>(q_pe) & 15u) ||
-      (reinterpret_cast<uintptr_t>(ckv_cache) & 15u) ||
-      (reinterpret_cast<uintptr_t>(kpe_cache) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u))
+  if (misaligned(workspace, 256)) return BIA_ERR_INVALID_ARG;
+  if (misaligned(q_nope, 16) || misaligned(q_pe, 16) || misaligned(ckv_cache, 16) ||
+      misaligned(kpe_cache, 16) || misaligned(out, 16) || misaligned(lse, 4) ||
+      misaligned(kv_indptr, 4) || misaligned(kv_indices, 4) || misaligned(kv_last_page_len, 4))
     return BIA_ERR_INVALID_ARG;
   if (split_size == 0) split_size = BIA_DECODE_SPLIT;
   HostPlan hp;
@@ -603,11 +618,17 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
   if (ce == 0) ce = encode_2d_map(&a.tm_kpe, kpe_cache, kv_rows, BIA_MLA_KPE_DIM, 1);
   if (ce != 0) return fail(BIA_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable", ce);
   const bool profile = g_attn_begin != nullptr && g_attn_end != nullptr;
-  if (profile && cudaEventRecord(g_attn_begin, st) != cudaSuccess) return BIA_ERR_CUDA;
+  if (profile) {
+    const cudaError_t re = cudaEventRecord(g_attn_begin, st);
+    if (re != cudaSuccess) return cuda_fail("profile event record", re);
+  }
   e = bia::launch_mla_decode(a, st);
   if (e != cudaSuccess) return cuda_fail("mla decode kernel launch", e);
   __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
-  if (profile && cudaEventRecord(g_attn_end, st) != cudaSuccess) return BIA_ERR_CUDA;
+  if (profile) {
+    const cudaError_t re = cudaEventRecord(g_attn_end, st);
+    if (re != cudaSuccess) return cuda_fail("profile event record", re);
+  }
   if (hp.part_rows > 0) {
     e = bia::launch_merge_partials(a, st);
     if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);

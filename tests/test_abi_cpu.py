@@ -89,16 +89,17 @@ FAKE = 1 << 20  # a 256-byte aligned address that is never dereferenced
 
 
 def call_prefill(bia, desc, qo, kvp, last, *, causal=1, split=0, ws_bytes=1 << 30, ws=FAKE,
-                 num_pages=1 << 20):
+                 num_pages=1 << 20, lse=None, kv_indices=FAKE):
     lib = bia.load()
     qo = torch.tensor(qo, dtype=torch.int32)
     kvp = torch.tensor(kvp, dtype=torch.int32)
     last = torch.tensor(last, dtype=torch.int32)
     p = ctypes.c_void_p
     return lib.bia_prefill_paged(ctypes.byref(desc), p(FAKE), p(FAKE), p(FAKE), num_pages,
-                                 p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(qo.data_ptr()),
+                                 p(FAKE), p(FAKE), p(kv_indices), p(FAKE), p(qo.data_ptr()),
                                  p(kvp.data_ptr()), p(last.data_ptr()), len(qo) - 1, causal,
-                                 split, p(ws), ws_bytes, p(FAKE), None, None)
+                                 split, p(ws), ws_bytes, p(FAKE), None if lse is None else p(lse),
+                                 None)
 
 
 def test_prefill_rejects_bad_arguments_on_the_host(bia):
@@ -116,6 +117,8 @@ def test_prefill_rejects_bad_arguments_on_the_host(bia):
     assert call_prefill(bia, d, [0, 10], [0, 10], [1], ws_bytes=300) == small
     assert call_prefill(bia, d, [0, 10], [0, 10], [1], ws=FAKE + 16) == inv  # unaligned
     assert call_prefill(bia, d, [0, 10], [0, 10], [1], num_pages=0) == inv
+    assert call_prefill(bia, d, [0, 10], [0, 10], [1], lse=FAKE + 2) == inv  # unaligned lse
+    assert call_prefill(bia, d, [0, 10], [0, 10], [1], kv_indices=FAKE + 1) == inv
     lib = bia.load()
     args = [None] * 20
     args[4], args[12], args[13], args[14], args[16] = 0, 0, 0, 0, 0
@@ -136,6 +139,10 @@ def test_decode_and_merge_reject_bad_arguments_on_the_host(bia):
                                 None) == bia.BIA_ERR_UNSUPPORTED
     assert lib.bia_merge_states(p(FAKE + 4), p(FAKE), None, 4, 2, 8, 128, p(FAKE), None,
                                 None) == bia.BIA_ERR_INVALID_ARG
+    assert lib.bia_merge_states(p(FAKE), p(FAKE + 2), None, 4, 2, 8, 128, p(FAKE), None,
+                                None) == bia.BIA_ERR_INVALID_ARG  # unaligned lse of the states
+    assert lib.bia_merge_states(p(FAKE), p(FAKE), p(FAKE + 1), 4, 2, 8, 128, p(FAKE), None,
+                                None) == bia.BIA_ERR_INVALID_ARG  # unaligned counts
     assert lib.bia_merge_states(None, None, None, 0, 2, 8, 128, None, None, None) == bia.BIA_OK
 
 
