@@ -239,6 +239,43 @@ BIA_API size_t bia_mla_decode_workspace_size(const bia_mla_desc *desc,
                                      int32_t split_size);
 
 /*
+ * Causal MLA extend (chunked prefill) over the same paged latent cache: the
+ * MLA counterpart of bia_prefill_paged, which the pages leave open ("sglang
+ * PR #43612", Summary: the flashinfer MLA path has no deterministic mode).
+ * Request b's q tokens are the last q_len = qo_indptr[b+1] - qo_indptr[b]
+ * positions of its kv_len keys (the rule of bia_prefill_paged); in-call token
+ * t sees keys 0 .. kv_len - q_len + t.
+ *   q_nope [total_q, num_heads, 512] bf16, q_pe [total_q, num_heads, 64] bf16
+ *   out    [total_q, num_heads, 512] bf16, lse [total_q, num_heads] fp32 or NULL
+ *   split_size: keys per split-KV tile, a multiple of 128; 0 = BIA_PREFILL_SPLIT
+ * Each q token runs as its own query against its own keys (the decode
+ * kernel's fixed split tiles and ascending merge), so its bits depend only on
+ * its request's keys up to its position and on split_size: the same in any
+ * batch and under any chunking of the extend, on the q-tile grid or off it;
+ * with equal split_size a token's bits equal those of bia_mla_decode_paged
+ * for that position.  A request may have q_len = 0.  total_q * num_heads and
+ * num_pages * page_size must stay below 2^31 (else BIA_ERR_UNSUPPORTED).
+ * Arguments, ownership and errors otherwise as for bia_prefill_paged
+ * (causal only).  The keys are read once per q token: this path suits short
+ * extends (speculative tokens, small chunks), not long prompts.
+ */
+BIA_API int bia_mla_prefill_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
+                          const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
+                          const int32_t *qo_indptr, const int32_t *kv_indptr,
+                          const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                          const int32_t *qo_indptr_host, const int32_t *kv_indptr_host,
+                          const int32_t *kv_last_page_len_host, int32_t batch, int32_t split_size,
+                          void *workspace, size_t workspace_bytes, void *out, float *lse,
+                          void *stream);
+
+/* Workspace bytes bia_mla_prefill_paged needs for this call (0 on invalid input). */
+BIA_API size_t bia_mla_prefill_workspace_size(const bia_mla_desc *desc,
+                                      const int32_t *qo_indptr_host,
+                                      const int32_t *kv_indptr_host,
+                                      const int32_t *kv_last_page_len_host, int32_t batch,
+                                      int32_t split_size);
+
+/*
  * Fixed-order log-sum-exp merge of attention states (the merge the split-KV
  * partials of "sglang PR #10417", Modifications, need; the pages fix only
  * that its order is fixed).  For row (i, h) the states s = 0..count-1 are

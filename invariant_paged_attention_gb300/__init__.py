@@ -38,7 +38,8 @@ EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged"
            "bia_status_string", "bia_read_status", "bia_set_profile_events",
            "bia_launch_count", "bia_last_error", "bia_decode_paged_noalloc",
            "bia_append_paged_kv", "bia_prefill_paged_mask", "bia_mla_decode_paged",
-           "bia_mla_decode_workspace_size")
+           "bia_mla_decode_workspace_size", "bia_mla_prefill_paged",
+           "bia_mla_prefill_workspace_size")
 
 
 class BiaError(RuntimeError):
@@ -117,6 +118,11 @@ def load(path: str = LIB_PATH):
     lib.bia_mla_decode_paged.restype = ctypes.c_int
     lib.bia_mla_decode_workspace_size.argtypes = [mp, vp, vp, i32, i32]
     lib.bia_mla_decode_workspace_size.restype = sz
+    lib.bia_mla_prefill_paged.argtypes = [mp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, vp,
+                                          i32, i32, vp, sz, vp, vp, vp]
+    lib.bia_mla_prefill_paged.restype = ctypes.c_int
+    lib.bia_mla_prefill_workspace_size.argtypes = [mp, vp, vp, vp, i32, i32]
+    lib.bia_mla_prefill_workspace_size.restype = sz
     _lib = lib
     return lib
 
@@ -424,3 +430,38 @@ def bia_mla_decode_paged(desc, q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
     if rc != BIA_OK:
         raise BiaError(rc, "bia_mla_decode_paged")
+
+
+def bia_mla_prefill_workspace_size(desc, qo_indptr_host, kv_indptr_host, kv_last_page_len_host,
+                                   split_size=0) -> int:
+    qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
+                     _host_i32(kv_last_page_len_host))
+    return int(load().bia_mla_prefill_workspace_size(ctypes.byref(desc), _ptr(qo), _ptr(kvp),
+                                                     _ptr(last), len(qo) - 1, int(split_size)))
+
+
+def bia_mla_prefill_paged(desc, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr,
+                          kv_indices, kv_last_page_len, qo_indptr_host, kv_indptr_host,
+                          kv_last_page_len_host, workspace, out, lse=None, split_size=0,
+                          stream=None):
+    """Causal multi-head latent attention extend: q_nope / q_pe / out hold
+    total_q token rows (include/bia.h states the layouts and the rule)."""
+    ts = _check_types(("q_nope", q_nope, BF16), ("q_pe", q_pe, BF16),
+                      ("ckv_cache", ckv_cache, BF16), ("kpe_cache", kpe_cache, BF16),
+                      ("qo_indptr", qo_indptr, I32), ("kv_indptr", kv_indptr, I32),
+                      ("kv_indices", kv_indices, I32), ("kv_last_page_len", kv_last_page_len, I32),
+                      ("workspace", workspace, None), ("out", out, BF16), ("lse", lse, F32, True))
+    if kpe_cache.dim() < 1 or ckv_cache.dim() < 1 or kpe_cache.shape[0] != ckv_cache.shape[0]:
+        raise ValueError("ckv_cache and kpe_cache must have the same number of pages")
+    _check_rows(q_nope, out, lse, "q_nope")
+    _check_cuda(ts)
+    qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
+                     _host_i32(kv_last_page_len_host))
+    rc = load().bia_mla_prefill_paged(
+        ctypes.byref(desc), _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+        ckv_cache.shape[0], _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices),
+        _ptr(kv_last_page_len), _ptr(qo), _ptr(kvp), _ptr(last), len(qo) - 1, int(split_size),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_mla_prefill_paged")

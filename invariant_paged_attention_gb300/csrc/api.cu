@@ -500,61 +500,64 @@ int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void
 }
 
 namespace {
-// Multi-head latent attention decode: validation and plan sizes as for the
-// GQA decode, with one shared 512 + 64 wide latent "kv head".
-int mla_plan(const bia_mla_desc *d, const int32_t *kvp_host, const int32_t *last_host,
-             int32_t batch, int32_t split, HostPlan *hp, bia_attn_desc *as_attn) {
+// Multi-head latent attention: validation and plan sizes as for the GQA
+// decode (qo_host == nullptr, one query per request) or a causal extend of
+// one-token q tiles (qo_host given), with one shared 512 + 64 wide latent
+// "kv head".
+int mla_plan(const bia_mla_desc *d, const int32_t *qo_host, const int32_t *kvp_host,
+             const int32_t *last_host, int32_t batch, int32_t split, HostPlan *hp) {
   if (!d || d->page_size <= 0) return BIA_ERR_INVALID_ARG;
   if (d->num_heads <= 0 || d->num_heads % 8 != 0 || d->num_heads > 1024) return BIA_ERR_UNSUPPORTED;
   if (!is_pow2(d->page_size) || d->page_size > 256) return BIA_ERR_UNSUPPORTED;
   if (!std::isfinite(d->sm_scale)) return BIA_ERR_INVALID_ARG;
-  *as_attn = bia_attn_desc{d->num_heads, 1, BIA_MLA_CKV_DIM, d->page_size, d->sm_scale};
-  return host_plan(as_attn, nullptr, kvp_host, last_host, batch, 1, split, 1, 1, 1, 0, hp);
+  const bia_attn_desc as_attn{d->num_heads, 1, BIA_MLA_CKV_DIM, d->page_size, d->sm_scale};
+  return host_plan(&as_attn, qo_host, kvp_host, last_host, batch, 1, split, 1, 1, 1, 0, hp);
 }
-} // namespace
 
-size_t bia_mla_decode_workspace_size(const bia_mla_desc *desc, const int32_t *kv_indptr_host,
-                                     const int32_t *kv_last_page_len_host, int32_t batch,
-                                     int32_t split_size) {
-  if (split_size == 0) split_size = BIA_DECODE_SPLIT;
+size_t mla_workspace_size(const bia_mla_desc *desc, const int32_t *qo_host,
+                          const int32_t *kvp_host, const int32_t *last_host, int32_t batch,
+                          int32_t split) {
   HostPlan hp;
-  bia_attn_desc ad;
-  if (mla_plan(desc, kv_indptr_host, kv_last_page_len_host, batch, split_size, &hp, &ad) !=
-      BIA_OK)
-    return 0;
+  if (mla_plan(desc, qo_host, kvp_host, last_host, batch, split, &hp) != BIA_OK) return 0;
   return bia::make_layout(batch, hp.n_groups, hp.n_units, 0, hp.part_rows, desc->num_heads,
                           BIA_MLA_CKV_DIM)
       .total;
 }
 
-int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
-                         const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
-                         const int32_t *kv_indptr, const int32_t *kv_indices,
-                         const int32_t *kv_last_page_len, const int32_t *kv_indptr_host,
-                         const int32_t *kv_last_page_len_host, int32_t batch, int32_t split_size,
-                         void *workspace, size_t workspace_bytes, void *out, float *lse,
-                         void *stream) {
+// One MLA call: extend (qo_indptr given) or decode (qo_indptr == nullptr).
+int run_mla(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
+            const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
+            const int32_t *qo_indptr, const int32_t *kv_indptr, const int32_t *kv_indices,
+            const int32_t *kv_last_page_len, const int32_t *qo_host, const int32_t *kvp_host,
+            const int32_t *last_host, int32_t batch, int32_t split_size, void *workspace,
+            size_t workspace_bytes, void *out, float *lse, void *stream) {
+  const bool extend = qo_host != nullptr;
   if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indptr || !kv_indices ||
-      !kv_last_page_len || !out || !workspace || num_pages <= 0)
+      !kv_last_page_len || !out || !workspace || num_pages <= 0 || (extend && !qo_indptr))
     return BIA_ERR_INVALID_ARG;
   if (misaligned(workspace, 256)) return BIA_ERR_INVALID_ARG;
   if (misaligned(q_nope, 16) || misaligned(q_pe, 16) || misaligned(ckv_cache, 16) ||
       misaligned(kpe_cache, 16) || misaligned(out, 16) || misaligned(lse, 4) ||
-      misaligned(kv_indptr, 4) || misaligned(kv_indices, 4) || misaligned(kv_last_page_len, 4))
+      misaligned(qo_indptr, 4) || misaligned(kv_indptr, 4) || misaligned(kv_indices, 4) ||
+      misaligned(kv_last_page_len, 4))
     return BIA_ERR_INVALID_ARG;
-  if (split_size == 0) split_size = BIA_DECODE_SPLIT;
   HostPlan hp;
-  bia_attn_desc ad;
-  int rc = mla_plan(desc, kv_indptr_host, kv_last_page_len_host, batch, split_size, &hp, &ad);
+  int rc = mla_plan(desc, qo_host, kvp_host, last_host, batch, split_size, &hp);
   if (rc != BIA_OK) return rc;
   const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, 0, hp.part_rows,
                                       desc->num_heads, BIA_MLA_CKV_DIM);
   if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
+  if (hp.total_q == 0) return BIA_OK;
+  // tensor maps: the heads' q rows in 16-row boxes, the latent rows one row
+  // per box (gathered)
+  const int64_t q_rows = hp.total_q * desc->num_heads;
+  const int64_t kv_rows = num_pages * desc->page_size;
+  if (q_rows >= INT32_MAX || kv_rows >= INT32_MAX) return BIA_ERR_UNSUPPORTED;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   PlanArgs pa{};
-  pa.qo_indptr = nullptr;
+  pa.qo_indptr = extend ? qo_indptr : nullptr;
   pa.kv_indptr = kv_indptr;
   pa.kv_last_page_len = kv_last_page_len;
   pa.batch = batch;
@@ -582,6 +585,7 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
   a.k_cache = static_cast<const uint16_t *>(ckv_cache);
   a.kpe_cache = static_cast<const uint16_t *>(kpe_cache);
   a.kv_indices = kv_indices;
+  a.qo_indptr = pa.qo_indptr;
   a.num_pages = num_pages;
   a.Hq = desc->num_heads;
   a.Hkv = 1;
@@ -605,11 +609,6 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
   a.out = static_cast<uint16_t *>(out);
   a.lse = lse;
   a.status = pa.status;
-  // tensor maps: the heads' q rows in 16-row boxes, the latent rows one row
-  // per box (gathered)
-  const int64_t q_rows = static_cast<int64_t>(batch) * desc->num_heads;
-  const int64_t kv_rows = num_pages * desc->page_size;
-  if (q_rows >= INT32_MAX || kv_rows >= INT32_MAX) return BIA_ERR_UNSUPPORTED;
   a.q_rows = static_cast<int32_t>(q_rows);
   a.kv_rows = static_cast<int32_t>(kv_rows);
   int ce = encode_2d_map(&a.tm_q, q_nope, q_rows, BIA_MLA_CKV_DIM, bia::kMlaHeadGroup);
@@ -623,8 +622,8 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
     if (re != cudaSuccess) return cuda_fail("profile event record", re);
   }
   e = bia::launch_mla_decode(a, st);
-  if (e != cudaSuccess) return cuda_fail("mla decode kernel launch", e);
-  __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  if (e != cudaSuccess) return cuda_fail("mla kernel launch", e);
+  if (hp.n_units > 0) __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   if (profile) {
     const cudaError_t re = cudaEventRecord(g_attn_end, st);
     if (re != cudaSuccess) return cuda_fail("profile event record", re);
@@ -635,6 +634,51 @@ int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const voi
     __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   }
   return BIA_OK;
+}
+} // namespace
+
+size_t bia_mla_decode_workspace_size(const bia_mla_desc *desc, const int32_t *kv_indptr_host,
+                                     const int32_t *kv_last_page_len_host, int32_t batch,
+                                     int32_t split_size) {
+  return mla_workspace_size(desc, nullptr, kv_indptr_host, kv_last_page_len_host, batch,
+                            split_size == 0 ? BIA_DECODE_SPLIT : split_size);
+}
+
+int bia_mla_decode_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
+                         const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
+                         const int32_t *kv_indptr, const int32_t *kv_indices,
+                         const int32_t *kv_last_page_len, const int32_t *kv_indptr_host,
+                         const int32_t *kv_last_page_len_host, int32_t batch, int32_t split_size,
+                         void *workspace, size_t workspace_bytes, void *out, float *lse,
+                         void *stream) {
+  return run_mla(desc, q_nope, q_pe, ckv_cache, kpe_cache, num_pages, nullptr, kv_indptr,
+                 kv_indices, kv_last_page_len, nullptr, kv_indptr_host, kv_last_page_len_host,
+                 batch, split_size == 0 ? BIA_DECODE_SPLIT : split_size, workspace,
+                 workspace_bytes, out, lse, stream);
+}
+
+size_t bia_mla_prefill_workspace_size(const bia_mla_desc *desc, const int32_t *qo_indptr_host,
+                                      const int32_t *kv_indptr_host,
+                                      const int32_t *kv_last_page_len_host, int32_t batch,
+                                      int32_t split_size) {
+  if (!qo_indptr_host) return 0;
+  return mla_workspace_size(desc, qo_indptr_host, kv_indptr_host, kv_last_page_len_host, batch,
+                            split_size == 0 ? BIA_PREFILL_SPLIT : split_size);
+}
+
+int bia_mla_prefill_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
+                          const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
+                          const int32_t *qo_indptr, const int32_t *kv_indptr,
+                          const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                          const int32_t *qo_indptr_host, const int32_t *kv_indptr_host,
+                          const int32_t *kv_last_page_len_host, int32_t batch, int32_t split_size,
+                          void *workspace, size_t workspace_bytes, void *out, float *lse,
+                          void *stream) {
+  if (!qo_indptr_host) return BIA_ERR_INVALID_ARG;
+  return run_mla(desc, q_nope, q_pe, ckv_cache, kpe_cache, num_pages, qo_indptr, kv_indptr,
+                 kv_indices, kv_last_page_len, qo_indptr_host, kv_indptr_host,
+                 kv_last_page_len_host, batch, split_size == 0 ? BIA_PREFILL_SPLIT : split_size,
+                 workspace, workspace_bytes, out, lse, stream);
 }
 
 int32_t bia_q_tile_tokens(int32_t gqa_group) {

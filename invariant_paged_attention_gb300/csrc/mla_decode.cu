@@ -12,8 +12,12 @@
 // 16 to 128 heads, far fewer than the 128 rows of an M=128 tile, while a
 // 128-key block fills M exactly.
 //
-// One CTA per (request, split tile, group of 16 heads); keys in 128-key
-// blocks.  Per block:
+// One CTA per (query token, split tile, group of 16 heads); keys in 128-key
+// blocks.  A decode call has one query token per request; an extend call
+// (bia_mla_prefill_paged) runs each of its causal query tokens the same way,
+// against the keys up to its own position, so a token's bits depend only on
+// its request's keys and the split size: not on the batch, and not on how
+// the extend is chunked.  Per block:
 //   S^T = C Q^T     M=128 keys, N=16 heads, K=512+64: A = the latent rows
 //                   (K-major, 64-column SW128 pieces), B = the 16 heads'
 //                   q_nope / q_pe (K-major), fp32 accumulator in TMEM
@@ -123,8 +127,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   if (u.b < 0) return;
   const ReqInfo r = a.reqs[u.b];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // u.tile: the query token's index within its request (0 for a decode
+  // query); causal, so token tq sees keys 0 .. kv_len - q_len + tq
+  const int32_t tq = u.tile;
+  const int32_t kv_end = r.kv_len - r.q_len + tq + 1;
+  const int64_t q_token = static_cast<int64_t>(r.q_start) + tq;
   const int32_t key_begin = u.split * a.split;
-  const int32_t key_end = min(key_begin + a.split, r.kv_len);
+  const int32_t key_end = min(key_begin + a.split, kv_end);
   const int nb = key_end > key_begin ? (key_end - key_begin + kKeys - 1) / kKeys : 0;
   const int h_real = min(kHg, a.Hq - hg * kHg); // heads of this group (the rest are padding)
 
@@ -154,7 +163,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   if (warp >= kProdWarpT) {
     // ------------------------------------------------------------ producers
     const int pt = tid - kProdWarpT * 32; // 0..127
-    const int32_t q_row = r.q_start * a.Hq + hg * kHg; // rows past B*H read as zeros
+    // rows past total_q * H read as zeros
+    const int32_t q_row = static_cast<int32_t>(q_token * a.Hq + hg * kHg);
     if (pt == 0 && nb > 0) {
       mbar_expect_tx(bar(L::bQFull), 9u * L::kQPiece);
       for (int p = 0; p < kCkvPieces; ++p)
@@ -436,9 +446,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       const float lse = nz[h] ? __fmul_rn(__fadd_rn(m[h], lg2(ls)), kLn2) : -INFINITY;
       lse_mine = t == h ? lse : lse_mine;
     }
-    const bool single = (r.kv_len - 1) / a.split == 0; // one split: the final row
-    const int64_t head0 = static_cast<int64_t>(r.q_start) * a.Hq + hg * kHg + h0;
-    const int64_t prow0 = (r.rowbase + u.split) * a.Hq + hg * kHg + h0;
+    const bool single = (kv_end - 1) / a.split == 0; // one split: the final row
+    const int64_t head0 = q_token * a.Hq + hg * kHg + h0;
+    const int64_t prow0 =
+        (r.rowbase + static_cast<int64_t>(tq) * r.nsp + u.split) * a.Hq + hg * kHg + h0;
 #pragma unroll
     for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
       uint32_t o[kHs];

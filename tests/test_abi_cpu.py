@@ -178,3 +178,38 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             m.load(str(tmp_path / "missing.so"))
     finally:
         m._lib = saved
+
+
+def test_mla_extend_rejects_bad_arguments_on_the_host(bia):
+    lib = bia.load()
+    p = ctypes.c_void_p
+
+    def call(desc, qo, kvp, last, split=0, ws_bytes=1 << 30, qo_host=True):
+        qo, kvp, last = (torch.tensor(x, dtype=torch.int32) for x in (qo, kvp, last))
+        return lib.bia_mla_prefill_paged(
+            ctypes.byref(desc), p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1 << 20, p(FAKE), p(FAKE),
+            p(FAKE), p(FAKE), p(qo.data_ptr()) if qo_host else None, p(kvp.data_ptr()),
+            p(last.data_ptr()), len(kvp) - 1, split, p(FAKE), ws_bytes, p(FAKE), None, None)
+    d = bia.make_mla_desc(16, 16)
+    inv = bia.BIA_ERR_INVALID_ARG
+    assert call(d, [0, 17], [0, 1], [16]) == inv  # 17 q tokens, 16 keys
+    assert call(d, [1, 2], [0, 1], [16]) == inv  # qo_indptr[0] != 0
+    assert call(d, [0, 3, 2], [0, 1, 2], [16, 16]) == inv  # decreasing qo_indptr
+    assert call(d, [0, 1], [0, 1], [16], qo_host=False) == inv
+    assert call(d, [0, 1], [0, 1], [16], split=100) == bia.BIA_ERR_UNSUPPORTED
+    assert call(bia.make_mla_desc(12, 16), [0, 1], [0, 1], [16]) == bia.BIA_ERR_UNSUPPORTED
+    assert call(d, [0, 1], [0, 1], [16], ws_bytes=16) == bia.BIA_ERR_WORKSPACE_TOO_SMALL
+    # no q token anywhere: nothing is enqueued
+    assert call(d, [0, 0, 0], [0, 1, 3], [5, 2]) == bia.BIA_OK
+
+
+def test_mla_extend_workspace_counts_token_partials(bia):
+    d = bia.make_mla_desc(16, 16)
+    # 20 tokens at positions 4090..4109: none reaches a second 8192-key split
+    # tile; with the default 4096 the last 14 do, so the request has 2 splits
+    one = bia.bia_mla_prefill_workspace_size(d, [0, 20], [0, 257], [14], 8192)
+    two = bia.bia_mla_prefill_workspace_size(d, [0, 20], [0, 257], [14])
+    # partial rows: 20 tokens x 2 splits x 16 heads x (512 + 1) fp32
+    assert two - one >= 20 * 2 * 16 * 513 * 4
+    assert bia.bia_mla_prefill_workspace_size(d, [0, 20], [0, 257], [14], 100) == 0
+    assert bia.bia_mla_prefill_workspace_size(d, [0, 20], [0, 1], [14]) == 0  # 20 > 14 keys

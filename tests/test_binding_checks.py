@@ -156,3 +156,23 @@ def test_mla_checks():
 def test_read_status_wants_a_device_workspace():
     with pytest.raises(ValueError, match="workspace must be a CUDA tensor"):
         bia.bia_read_status(torch.zeros(256, dtype=torch.uint8))
+
+
+def test_mla_extend_checks():
+    args = dict(desc=bia.make_mla_desc(16, 16), q_nope=torch.zeros(5, 16, 512, dtype=BF16),
+                q_pe=torch.zeros(5, 16, 64, dtype=BF16),
+                ckv_cache=torch.zeros(4, 16, 512, dtype=BF16),
+                kpe_cache=torch.zeros(4, 16, 64, dtype=BF16),
+                qo_indptr=torch.tensor([0, 2, 5], dtype=I32),
+                kv_indptr=torch.tensor([0, 1, 2], dtype=I32),
+                kv_indices=torch.tensor([0, 1], dtype=I32),
+                kv_last_page_len=torch.tensor([3, 5], dtype=I32), qo_indptr_host=[0, 2, 5],
+                kv_indptr_host=[0, 1, 2], kv_last_page_len_host=[3, 5],
+                workspace=torch.zeros(256, dtype=torch.uint8),
+                out=torch.zeros(5, 16, 512, dtype=BF16), lse=torch.zeros(5, 16))
+    with pytest.raises(TypeError, match="qo_indptr must be"):
+        bia.bia_mla_prefill_paged(**{**args, "qo_indptr": torch.tensor([0, 2, 5])})
+    with pytest.raises(ValueError, match="lse must hold"):
+        bia.bia_mla_prefill_paged(**{**args, "lse": torch.zeros(2, 16)})
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bia.bia_mla_prefill_paged(**args)
