@@ -40,7 +40,11 @@
  * allocates device memory and never synchronises the stream.  The *_host
  * arrays are read synchronously during the call (to validate and to size the
  * launch) and must equal their device copies.  All work is enqueued on
- * `stream` (a cudaStream_t; NULL = legacy default stream).
+ * `stream` (a cudaStream_t; NULL = legacy default stream) on the current
+ * device.  A process drives one GPU: each kernel's shared-memory limit is
+ * raised on its first launch, for the device current then, and a later
+ * launch on another device fails with BIA_ERR_CUDA (one process per GPU is
+ * the intended deployment).
  *
  * Errors: every entry point returns BIA_OK or a negative bia_status and never
  * aborts.  Host-side checks run before anything is enqueued.  A page index
