@@ -500,6 +500,35 @@ def sweep_mla(wl, bia, dev, stream, time_calls, emit):
     del mst, mc, mws, mout
     torch.cuda.empty_cache()
 
+    # MLA extend: 64 requests each verifying 4 speculative tokens, same lengths
+    est = wl.MLAStore([wl.Sequence(7800 + i, c - 4, 4) for i, c in enumerate(ctx)], 16, 512,
+                      64, 1, dev, layout_seed=7998)
+    ec = wl.mla_call(est, [(i, 0, 4) for i in range(len(est.seqs))])
+    ews = torch.empty(bia.bia_mla_prefill_workspace_size(mdesc, ec.qo_indptr, ec.kv_indptr,
+                                                         ec.kv_last_page_len),
+                      dtype=torch.uint8, device=dev)
+    eout = torch.empty((int(ec.qo_indptr[-1]), 16, 512), dtype=torch.bfloat16, device=dev)
+    eargs = [ec.qo_indptr.to(dev), ec.kv_indptr.to(dev), ec.kv_indices.to(dev),
+             ec.kv_last_page_len.to(dev)]
+
+    def mla_ext_f(evs):
+        if evs:
+            bia.bia_set_profile_events(*evs)
+        bia.bia_mla_prefill_paged(mdesc, ec.q_nope, ec.q_pe, est.ckv_cache, est.kpe_cache,
+                                  *eargs, ec.qo_indptr, ec.kv_indptr, ec.kv_last_page_len, ews,
+                                  eout, stream=stream)
+        if evs:
+            bia.bia_set_profile_events(None, None)
+    cm, km = time_calls([mla_ext_f])
+    # token t of a request sees kv_len - 3 + t keys; 2 flops per multiply-add
+    # over 576 score columns and 512 value columns, 16 heads
+    visible = sum(4 * kv - 6 for kv in ec.kv_lens)
+    emit("MLA extend B=64 x 4 tokens, 16 heads, latent 512+64 (ctx U[1024,32768], page 1)",
+         "prefill", visible * 16 * 2 * (576 + 512), cm, km,
+         {"latent_bytes_per_token_pass": visible * (512 + 64) * 2})
+    del est, ec, ews, eout
+    torch.cuda.empty_cache()
+
 
 def main():
     args = parse_args()
