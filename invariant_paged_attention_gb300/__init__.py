@@ -164,7 +164,17 @@ def _check_types(*specs):
     return given
 
 
-def _check_cuda(given):
+def _launch_device(stream) -> torch.device:
+    """The device the library enqueues on: a torch stream's own device, else
+    the current one (a raw cudaStream_t handle is taken to belong to it)."""
+    dev = getattr(stream, "device", None)
+    if isinstance(dev, torch.device) and dev.type == "cuda":
+        return torch.device("cuda", dev.index if dev.index is not None else
+                            torch.cuda.current_device())
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _check_cuda(given, stream=None):
     device = None
     for name, t in given:
         if t.device.type != "cuda":
@@ -173,6 +183,11 @@ def _check_cuda(given):
             device = t.device
         elif t.device != device:
             raise ValueError(f"{name} is on {t.device}, the other arguments on {device}")
+    if device is not None:
+        want = _launch_device(stream)
+        have = torch.device("cuda", device.index if device.index is not None else want.index)
+        if have != want:
+            raise ValueError(f"the tensors are on {have} but the work would run on {want}")
 
 
 def _check_rows(q, out, lse, qname="q"):
@@ -239,7 +254,7 @@ def bia_prefill_paged(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indice
                       ("workspace", workspace, None), ("out", out, BF16), ("lse", lse, F32, True))
     _check_caches(k_cache, v_cache)
     _check_rows(q, out, lse)
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
                      _host_i32(kv_last_page_len_host))
     rc = load().bia_prefill_paged(
@@ -265,7 +280,7 @@ def bia_prefill_paged_mask(desc, q, k_cache, v_cache, qo_indptr, kv_indptr, kv_i
                       ("workspace", workspace, None), ("out", out, BF16), ("lse", lse, F32, True))
     _check_caches(k_cache, v_cache)
     _check_rows(q, out, lse)
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
                      _host_i32(kv_last_page_len_host))
     mih = torch.as_tensor(mask_indptr_host, dtype=torch.int64).contiguous()
@@ -290,7 +305,7 @@ def bia_decode_paged(desc, q, k_cache, v_cache, kv_indptr, kv_indices, kv_last_p
                       ("out", out, BF16), ("lse", lse, F32, True))
     _check_caches(k_cache, v_cache)
     _check_rows(q, out, lse)
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
     rc = load().bia_decode_paged(
         ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -316,7 +331,7 @@ def bia_decode_paged_noalloc(desc, q, k_cache, v_cache, kv_indptr, kv_indices, k
                       ("lse", lse, F32, True))
     _check_caches(k_cache, v_cache)
     _check_rows(q, out, lse)
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
     rc = load().bia_decode_paged_noalloc(
         ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -339,7 +354,7 @@ def bia_append_paged_kv(desc, k_new, v_new, k_cache, v_cache, append_indptr, kv_
     _check_caches(k_cache, v_cache)
     if tuple(v_new.shape) != tuple(k_new.shape):
         raise ValueError(f"v_new has shape {tuple(v_new.shape)}, k_new {tuple(k_new.shape)}")
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     ap, kvp, last = (_host_i32(append_indptr_host), _host_i32(kv_indptr_host),
                      _host_i32(kv_last_page_len_host))
     rc = load().bia_append_paged_kv(
@@ -365,7 +380,7 @@ def bia_merge_states(v, s, out, out_lse=None, num_states=None, stream=None):
         raise ValueError(f"out_lse must be {(n, H)}, got {tuple(out_lse.shape)}")
     if num_states is not None and num_states.numel() != n:
         raise ValueError(f"num_states must hold {n} counts, got {num_states.numel()}")
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     rc = load().bia_merge_states(_ptr(v), _ptr(s), _ptr(num_states), n, S, H, D, _ptr(out),
                                  _ptr(out_lse), _stream(stream))
     if rc != BIA_OK:
@@ -374,7 +389,7 @@ def bia_merge_states(v, s, out, out_lse=None, num_states=None, stream=None):
 
 def bia_read_status(workspace, stream=None) -> int:
     ts = _check_types(("workspace", workspace, None))
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     st = ctypes.c_int32(0)
     rc = load().bia_read_status(_ptr(workspace), ctypes.byref(st), _stream(stream))
     if rc != BIA_OK:
@@ -421,7 +436,7 @@ def bia_mla_decode_paged(desc, q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv
     if kpe_cache.dim() < 1 or ckv_cache.dim() < 1 or kpe_cache.shape[0] != ckv_cache.shape[0]:
         raise ValueError("ckv_cache and kpe_cache must have the same number of pages")
     _check_rows(q_nope, out, lse, "q_nope")
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     kvp, last = _host_i32(kv_indptr_host), _host_i32(kv_last_page_len_host)
     rc = load().bia_mla_decode_paged(
         ctypes.byref(desc), _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
@@ -454,7 +469,7 @@ def bia_mla_prefill_paged(desc, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, k
     if kpe_cache.dim() < 1 or ckv_cache.dim() < 1 or kpe_cache.shape[0] != ckv_cache.shape[0]:
         raise ValueError("ckv_cache and kpe_cache must have the same number of pages")
     _check_rows(q_nope, out, lse, "q_nope")
-    _check_cuda(ts)
+    _check_cuda(ts, stream)
     qo, kvp, last = (_host_i32(qo_indptr_host), _host_i32(kv_indptr_host),
                      _host_i32(kv_last_page_len_host))
     rc = load().bia_mla_prefill_paged(

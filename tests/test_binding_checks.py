@@ -176,3 +176,20 @@ def test_mla_extend_checks():
         bia.bia_mla_prefill_paged(**{**args, "lse": torch.zeros(2, 16)})
     with pytest.raises(ValueError, match="CUDA tensor"):
         bia.bia_mla_prefill_paged(**args)
+
+
+def test_tensors_must_sit_on_the_launch_device(monkeypatch):
+    from types import SimpleNamespace as NS
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    on = lambda i: NS(device=torch.device("cuda", i))  # noqa: E731
+    bia._check_cuda([("q", on(0)), ("out", on(0))])  # the current device: fine
+    with pytest.raises(ValueError, match="the other arguments on cuda:0"):
+        bia._check_cuda([("q", on(0)), ("out", on(1))])
+    with pytest.raises(ValueError, match="would run on cuda:0"):
+        bia._check_cuda([("q", on(1)), ("out", on(1))])
+    # a stream of device 1 takes the work there
+    bia._check_cuda([("q", on(1))], stream=NS(device=torch.device("cuda", 1)))
+    with pytest.raises(ValueError, match="would run on cuda:1"):
+        bia._check_cuda([("q", on(0))], stream=NS(device=torch.device("cuda", 1)))
+    # a raw stream handle belongs to the current device
+    bia._check_cuda([("q", on(0))], stream=12345)
