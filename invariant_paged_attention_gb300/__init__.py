@@ -9,9 +9,9 @@ The functions carry the C names of ``include/bia.h`` and take torch tensors:
 device tensors for the data and the device copies of the index arrays, CPU
 int32 tensors for the host mirrors.  Before a call reaches the library, its
 device tensors are checked for dtype, contiguity, the shapes the passed sizes
-come from and one common CUDA device (TypeError / ValueError); everything
-else (descriptor, index arrays, workspace size) is checked by the library
-itself, which raises BiaError with its status code.
+come from and the CUDA device the call enqueues on (TypeError / ValueError);
+everything else (descriptor, index arrays, workspace size) is checked by the
+library itself, which raises BiaError with its status code.
 """
 from __future__ import annotations
 
