@@ -213,3 +213,25 @@ def test_mla_extend_workspace_counts_token_partials(bia):
     assert two - one >= 20 * 2 * 16 * 513 * 4
     assert bia.bia_mla_prefill_workspace_size(d, [0, 20], [0, 257], [14], 100) == 0
     assert bia.bia_mla_prefill_workspace_size(d, [0, 20], [0, 1], [14]) == 0  # 20 > 14 keys
+
+
+def test_sizes_past_the_32_bit_limits_are_refused_on_the_host(bia):
+    """The limits include/bia.h states: keys per request below 2^30, and for
+    the prefill / MLA tensor maps fewer than 2^31 key rows; refused before
+    anything is enqueued (the pointers here are never dereferenced)."""
+    d = bia.make_desc(32, 8, 128, 1)
+    uns = bia.BIA_ERR_UNSUPPORTED
+    # one request of 2^30 + 1 keys
+    assert call_prefill(bia, d, [0, 1], [0, (1 << 30) + 1], [1]) == uns
+    # 2^28 pages x 1 key x 8 kv heads = 2^31 rows of the K/V tensor maps
+    assert call_prefill(bia, d, [0, 10], [0, 10], [1], num_pages=1 << 28) == uns
+    lib = bia.load()
+    p = ctypes.c_void_p
+    md = bia.make_mla_desc(16, 1)
+    kvp = torch.tensor([0, 10], dtype=torch.int32)
+    last = torch.tensor([1], dtype=torch.int32)
+    rc = lib.bia_mla_decode_paged(ctypes.byref(md), p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1 << 31,
+                                  p(FAKE), p(FAKE), p(FAKE), p(kvp.data_ptr()),
+                                  p(last.data_ptr()), 1, 0, p(FAKE), 1 << 30, p(FAKE), None,
+                                  None)
+    assert rc == uns
