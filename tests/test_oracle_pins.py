@@ -315,3 +315,29 @@ def test_merge_closed_forms():
     # num_states limits the fold; zero states -> 0 / -inf
     o5, l5 = oracle.merge_states(v, s, num_states=[2, 0, 4])
     assert np.array_equal(o5[0], o4[0]) and np.all(o5[1] == 0) and np.all(l5[1] == -np.inf)
+
+
+def test_merge_is_order_free_associative_and_shift_stable():
+    """What the log-sum-exp merge fixes mathematically: the result does not
+    depend on the order of the states, merging merged groups gives the merge
+    of all, and shifting every lse by c shifts the result's lse by c and
+    leaves the output alone (no overflow at large lse)."""
+    rng = np.random.default_rng(11)
+    n, S, H, D = 5, 7, 3, 16
+    v = rng.standard_normal((n, S, H, D)).astype(np.float32)
+    s = (rng.integers(-24, 24, (n, S, H)) / 8.0).astype(np.float32)  # exact in fp32
+    out, lse = oracle.merge_states(v, s)
+    perm = rng.permutation(S)
+    po, pl = oracle.merge_states(v[:, perm], s[:, perm])
+    assert np.max(np.abs(po - out)) <= 1e-12 and np.max(np.abs(pl - lse)) <= 1e-12
+    # two groups merged first (their states rounded to fp32), then merged
+    ao, al = oracle.merge_states(v[:, :3], s[:, :3])
+    bo, bl = oracle.merge_states(v[:, 3:], s[:, 3:])
+    gv = np.stack([ao, bo], 1).astype(np.float32)
+    gs = np.stack([al, bl], 1).astype(np.float32)
+    go, gl = oracle.merge_states(gv, gs)
+    assert np.max(np.abs(go - out)) <= 1e-6 and np.max(np.abs(gl - lse)) <= 1e-6
+    # every lse shifted by 4096 (exact in fp32 for these values)
+    so, sl = oracle.merge_states(v, s + np.float32(4096.0))
+    assert np.all(np.isfinite(so)) and np.max(np.abs(so - out)) <= 1e-12
+    assert np.max(np.abs(sl - (lse + 4096.0))) <= 1e-9
