@@ -341,3 +341,41 @@ def test_merge_is_order_free_associative_and_shift_stable():
     so, sl = oracle.merge_states(v, s + np.float32(4096.0))
     assert np.all(np.isfinite(so)) and np.max(np.abs(so - out)) <= 1e-12
     assert np.max(np.abs(sl - (lse + 4096.0))) <= 1e-9
+
+
+def test_key_shift_and_value_affine_invariance():
+    """Softmax ignores a score offset that every key of a row shares: adding
+    one vector c to every key leaves the output alone and moves lse by
+    scale * <q, c>.  The output is affine in the values (the weights sum to
+    one): V -> 2 V + b gives 2 out + b.  Small integers keep every input exact
+    in bf16."""
+    Hq, Hkv, D, P = 4, 2, 16, 4
+    G = Hq // Hkv
+    store = wl.PagedStore([wl.Sequence(70, 5, 9), wl.Sequence(71, 0, 12)], Hq, Hkv, D, P, "cpu",
+                          layout_seed=13)
+    call = wl.whole_prefill(store)
+    g = torch.Generator().manual_seed(3)
+
+    def rint(shape, lo=-3, hi=4):
+        return torch.randint(lo, hi, tuple(shape), generator=g).to(torch.bfloat16)
+    call.q = rint(call.q.shape)
+    store.k_cache = rint(store.k_cache.shape)
+    store.v_cache = rint(store.v_cache.shape)
+    out, lse = oracle_on_call(call)
+
+    c = rint((Hkv, D))
+    k0 = store.k_cache
+    store.k_cache = (k0.float() + c.float()).to(torch.bfloat16)  # |values| <= 6: exact
+    so, sl = oracle_on_call(call)
+    store.k_cache = k0
+    q = call.q.float().numpy().astype(np.float64)
+    cq = np.stack([q[:, h] @ c.float().numpy()[h // G] for h in range(Hq)], 1)
+    assert np.max(np.abs(so - out)) <= 1e-12
+    assert np.max(np.abs(sl - (lse + cq / math.sqrt(D)))) <= 1e-12
+
+    b = rint((Hkv, D))
+    store.v_cache = (2 * store.v_cache.float() + b.float()).to(torch.bfloat16)
+    ao, al = oracle_on_call(call)
+    bb = np.stack([b.float().numpy()[h // G] for h in range(Hq)], 0)
+    assert np.max(np.abs(ao - (2 * out + bb[None]))) <= 1e-12
+    assert np.array_equal(al, lse)
