@@ -313,7 +313,8 @@ int oracle_row_probs(int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_di
         return ORACLE_BAD_ARG;
     oracle_problem pb = {num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, causal,
                          q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices,
-                         kv_last_page_len, batch, 0, INT64_MAX, NULL, 0, NULL, NULL};
+                         kv_last_page_len, batch, 0, INT64_MAX, NULL, 0, NULL, NULL,
+                         NULL, NULL};
     int b = owner_of_token(&pb, t);
     int64_t kv_len = request_kv_len(&pb, b);
     if (probs_len < kv_len)
