@@ -6,7 +6,6 @@ only: it may differ from the unchunked run."""
 import pytest
 import torch
 
-import invariant_paged_attention_gb300 as bia
 import workloads as wl
 from tests.gpu_util import check_rows, run_decode, run_prefill, same_bits
 

@@ -2,9 +2,7 @@
 kernel: one q tile per CTA, 64-key blocks): prefill and decode
 parity with the oracle, chunked prefill on the q-tile grid and batch
 composition bit-identical, and the append and masked paths at that width."""
-import numpy as np
 import pytest
-import torch
 
 import workloads as wl
 from tests.gpu_util import check_rows, run_decode, run_prefill, same_bits

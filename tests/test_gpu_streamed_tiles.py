@@ -6,7 +6,6 @@ a request chunked on the q-tile grid (its last chunk a single token)
 bit-identical to the unchunked run, whose tail tile is streamed the same
 way."""
 import pytest
-import torch
 
 import invariant_paged_attention_gb300 as bia
 import workloads as wl
