@@ -235,3 +235,25 @@ def test_sizes_past_the_32_bit_limits_are_refused_on_the_host(bia):
                                   p(last.data_ptr()), 1, 0, p(FAKE), 1 << 30, p(FAKE), None,
                                   None)
     assert rc == uns
+
+
+def test_binding_constants_match_the_header(bia):
+    """The numbers the binding mirrors from include/bia.h (split sizes, the
+    q-tile height, status codes, MLA widths, the static decode scratch)."""
+    import re
+    text = open(HEADER).read()
+    defines = {m.group(1): m.group(2) for m in
+               re.finditer(r"#define (BIA_[A-Z0-9_]+) (.+)", text)}
+    assert int(defines["BIA_Q_TILE_ROWS"]) == bia.BIA_Q_TILE_ROWS
+    assert int(defines["BIA_PREFILL_SPLIT"]) == bia.BIA_PREFILL_SPLIT
+    assert int(defines["BIA_DECODE_SPLIT"]) == bia.BIA_DECODE_SPLIT
+    assert int(defines["BIA_MLA_CKV_DIM"]) == bia.MLA_CKV_DIM
+    assert int(defines["BIA_MLA_KPE_DIM"]) == bia.MLA_KPE_DIM
+    assert defines["BIA_DECODE_NOALLOC_SCRATCH_BYTES"].strip() == "((size_t)64 << 20)"
+    assert bia.BIA_DECODE_NOALLOC_SCRATCH_BYTES == 64 << 20
+    codes = dict(re.findall(r"(BIA_(?:OK|ERR_[A-Z_]+)) = (-?\d+)", text))
+    assert {k: int(v) for k, v in codes.items()} == {
+        "BIA_OK": bia.BIA_OK, "BIA_ERR_INVALID_ARG": bia.BIA_ERR_INVALID_ARG,
+        "BIA_ERR_UNSUPPORTED": bia.BIA_ERR_UNSUPPORTED,
+        "BIA_ERR_WORKSPACE_TOO_SMALL": bia.BIA_ERR_WORKSPACE_TOO_SMALL,
+        "BIA_ERR_CUDA": bia.BIA_ERR_CUDA}
