@@ -99,6 +99,42 @@ def test_probabilities_form_a_distribution_and_respect_the_mask():
             assert np.all(p[pos + 1:] == 0.0)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,P,seqs,causal", SMALL)
+def test_probabilities_equal_the_dense_softmax_weights(Hq, Hkv, D, P, seqs, causal):
+    """Values of oracle_row_probs against numpy's dense softmax(q K^T * scale
+    + mask) row (keys gathered by fancy indexing, a different route): every
+    weight to 1e-12, and the weights times the dense V give the brute-force
+    output row.  A wrong scale, kv head, q row or mask offset fails here."""
+    store = wl.PagedStore([wl.Sequence(50 + i, p, n) for i, (p, n) in enumerate(seqs)],
+                          Hq, Hkv, D, P, "cpu", layout_seed=11)
+    call = wl.whole_prefill(store)
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(D)
+    q = call.q.float().numpy().astype(np.float64)
+    ref_out, _ = brute_force(call, causal=causal)
+    rng = np.random.default_rng(7)
+    for b, (kk, vv) in enumerate(dense_kv(call)):
+        q0, q1 = int(call.qo_indptr[b]), int(call.qo_indptr[b + 1])
+        if q1 == q0:
+            continue
+        kl = kk.shape[0]
+        for t in sorted({q0, q1 - 1, int(rng.integers(q0, q1))}):
+            for h in sorted({0, Hq - 1, int(rng.integers(0, Hq))}):
+                got = oracle.row_probs(
+                    wl.bf16_bits(call.q), wl.bf16_bits(store.k_cache), wl.bf16_bits(store.v_cache),
+                    call.qo_indptr.numpy(), call.kv_indptr.numpy(), call.kv_indices.numpy(),
+                    call.kv_last_page_len.numpy(), token=t, head=h, num_qo_heads=Hq,
+                    num_kv_heads=Hkv, head_dim=D, page_size=P, causal=causal)
+                pos = kl - (q1 - q0) + (t - q0)
+                s = (kk[:, h // G, :] @ q[t, h, :]) * scale
+                vis = np.arange(kl) <= pos if causal else np.ones(kl, bool)
+                e = np.where(vis, np.exp(s - s[vis].max()), 0.0)
+                want = e / e.sum()
+                assert got.shape == (kl,)
+                assert np.max(np.abs(got - want)) <= 1e-12
+                assert np.max(np.abs(got @ vv[:, h // G, :] - ref_out[t, h])) <= 1e-12
+
+
 def test_masked_keys_do_not_reach_a_row():
     """Overwrite every key/value after position p with huge values and NaN:
     row p must not change by a single bit."""
