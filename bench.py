@@ -8,14 +8,21 @@ followed by a decode call on the decode sweep's largest batch (256 requests,
 contexts uniform in [1024, 32768], page size 1, split-KV 2048).  Each call
 runs the device planner, the attention kernel and the split merge.
 
-Printed (rank 0, one JSON line): prefill algorithmic TFLOP/s as `value`
+Printed (one JSON line): prefill algorithmic TFLOP/s as `value`
 (causal-exact flops 4*D*sum(visible keys) over the prefill call time),
 decode K+V GB/s under `decode`, the attention kernels' rooflines against
-the measured peaks, an end-to-end number through host buffers, clocks
-sampled during the timed region, the number of kernel launches, and the CPU
-oracle timed on a bounded sample as a baseline.
+the measured peaks, end-to-end numbers of both calls through host buffers,
+clocks sampled during the timed region, the number of kernel launches, the
+CPU oracle timed on a bounded sample as a baseline, and under `configs` the
+other workloads (the prefix extend unchunked and in 256-token chunks, the
+mixed serving batch's prefill and decode calls, decode batches of 1, 8 and
+64), each call timed on its own with its kernel's roofline.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+The library drives one GPU per process: with --gpus other than 1, or under
+torchrun with several ranks, rank 0 prints a one-line `unavailable` record
+and no rank touches a GPU.
+
+  python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl ours|reference]
 """
 from __future__ import annotations
 
@@ -51,7 +58,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true",
                    help="skip the oracle CPU baseline (quick runs)")
-    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e legs")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads' legs (cfg3, cfg5, decode batches 1/8/64)")
     p.add_argument("--cpu-seconds", type=float, default=20.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--only", choices=["both", "prefill", "decode"], default="both",
@@ -105,20 +114,6 @@ def prefill_flops(call: wl.Call, D: int, Hq: int) -> int:
 
 def kv_bytes(call: wl.Call, Hkv: int, D: int) -> int:
     return sum(call.kv_lens) * Hkv * D * 2 * 2
-
-
-def aggregate_over_ranks(local_seconds, units_per_rank, steps, dist=None, device="cpu"):
-    """Whole-job throughput of N replicas: every rank contributes its summed
-    times, the slowest rank's time is the job's time (max over ranks), and the
-    job's work is the sum over ranks.  Returns (units per second, max seconds
-    per item of local_seconds)."""
-    t = torch.tensor(list(local_seconds), dtype=torch.float64, device=device)
-    w = torch.tensor([float(units_per_rank)], dtype=torch.float64, device=device)
-    if dist is not None and dist.is_initialized():
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(w, op=dist.ReduceOp.SUM)
-    tmax = t.tolist()
-    return (w.item() * steps / tmax[0] if tmax[0] > 0 else 0.0), tmax
 
 
 def source_hash(*files) -> str:
@@ -530,10 +525,80 @@ def sweep_mla(wl, bia, dev, stream, time_calls, emit):
     torch.cuda.empty_cache()
 
 
+class Leg:
+    """One call timed on its own: warm-up calls, then `steps` calls each
+    preceded by an untimed L2 flush (a 256 MiB write, more than the 129 MB
+    L2) and bracketed by CUDA events on the launching stream; the attention
+    kernel alone is timed by the events the library records around it."""
+
+    def __init__(self, bia, stream, flush):
+        self.bia, self.stream, self.flush = bia, stream, flush
+
+    def run(self, fns, steps, warmup):
+        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        for _ in range(warmup):
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        call_ms, kern_ms = [], []
+        launches0 = self.bia.bia_launch_count()
+        for _ in range(steps):
+            self.flush.zero_()
+            a0, a1, k0, k1 = ev(), ev(), ev(), ev()
+            if len(fns) == 1:
+                self.bia.bia_set_profile_events(k0, k1)
+            a0.record(self.stream)
+            for f in fns:
+                f()
+            a1.record(self.stream)
+            self.bia.bia_set_profile_events(None, None)
+            torch.cuda.synchronize()
+            call_ms.append(a0.elapsed_time(a1))
+            if len(fns) == 1:
+                kern_ms.append(k0.elapsed_time(k1))
+        launches = (self.bia.bia_launch_count() - launches0) // max(steps, 1)
+        return (statistics.median(call_ms), statistics.median(kern_ms) if kern_ms else None,
+                int(launches))
+
+
+def roofline_of(kind, work, kern_ms, peaks, peak_kind, kernel, traffic=None):
+    if kind == "tensor":
+        achieved = work / kern_ms / 1e9
+        return {"bound": "tensor", "kernel": kernel, "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "peak_source": f"bf16 dense burst, of {peak_kind}",
+                "algorithmic_flops_per_launch": work, "kernel_ms": kern_ms, "traffic": traffic}
+    achieved = work / kern_ms / 1e6
+    return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "peak_source": f"HBM copy, of {peak_kind}", "kv_bytes_per_launch": work,
+            "kernel_ms": kern_ms, "traffic": traffic}
+
+
+def refuse_multi_gpu(args, world, rank):
+    """The library runs on one GPU per process, and its prefill kernels
+    multicast K/V gathers inside thread-block clusters, which it does for one
+    GPU's own memory only: there is no multi-GPU bench.  Rank 0 says so in one
+    JSON line; every rank exits without touching a GPU."""
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "n_gpus": max(world, args.gpus),
+                          "unavailable": "one GPU only: the attention shards into independent "
+                                         "requests with no exchange step, and this library "
+                                         "runs on the GPU of the calling process alone"}),
+              flush=True)
+
+
 def main():
     args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         run_reference(args)
+        return
+    if world > 1 or args.gpus != 1:
+        refuse_multi_gpu(args, world, rank)
         return
     if args.sweep:
         run_sweep(args)
@@ -542,21 +607,11 @@ def main():
     import invariant_paged_attention_gb300 as bia
     from invariant_paged_attention_gb300 import build as bia_build
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
-    torch.cuda.set_device(local)
-    dev = f"cuda:{local}"
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device(dev))
-    if rank == 0 or world == 1:
-        bia_build.build()
-    if dist:
-        dist.barrier()
+    torch.cuda.set_device(0)
+    dev = "cuda:0"
+    bia_build.build()
     bia.load()
 
     # ---- inputs resident in HBM
@@ -568,45 +623,61 @@ def main():
         return [call.qo_indptr.to(dev), call.kv_indptr.to(dev), call.kv_indices.to(dev),
                 call.kv_last_page_len.to(dev)]
 
+    def prefill_call(store, call):
+        desc = bia.make_desc(store.num_qo_heads, store.num_kv_heads, store.head_dim,
+                             store.page_size)
+        qo, kvp, idx, last = dev_idx(call)
+        ws = torch.empty(bia.bia_prefill_workspace_size(desc, call.qo_indptr, call.kv_indptr,
+                                                        call.kv_last_page_len),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(call.q)
+        lse = torch.empty(call.total_q, store.num_qo_heads, dtype=torch.float32, device=dev)
+
+        def f(q=None, k=None, v=None, idx4=None):
+            bia.bia_prefill_paged(desc, call.q if q is None else q,
+                                  store.k_cache if k is None else k,
+                                  store.v_cache if v is None else v,
+                                  *(idx4 or (qo, kvp, idx, last)), call.qo_indptr,
+                                  call.kv_indptr, call.kv_last_page_len, ws, out, lse,
+                                  stream=stream)
+        f.out, f.lse = out, lse
+        return f
+
+    def decode_call(store, call):
+        desc = bia.make_desc(store.num_qo_heads, store.num_kv_heads, store.head_dim,
+                             store.page_size)
+        _, kvp, idx, last = dev_idx(call)
+        ws = torch.empty(bia.bia_decode_workspace_size(desc, call.kv_indptr,
+                                                       call.kv_last_page_len),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(call.q)
+        lse = torch.empty(call.total_q, store.num_qo_heads, dtype=torch.float32, device=dev)
+
+        def f(q=None, k=None, v=None, idx3=None):
+            bia.bia_decode_paged(desc, call.q if q is None else q,
+                                 store.k_cache if k is None else k,
+                                 store.v_cache if v is None else v,
+                                 *(idx3 or (kvp, idx, last)), call.kv_indptr,
+                                 call.kv_last_page_len, ws, out, lse, stream=stream)
+        f.out, f.lse = out, lse
+        return f
+
     flops = dbytes = 0
     prefill = decode = None
     if do_p:
         pstore = wl.cfg2_prefill(dev)
         pcall = wl.whole_prefill(pstore)
         Hq, Hkv, D = pstore.num_qo_heads, pstore.num_kv_heads, pstore.head_dim
-        pdesc = bia.make_desc(Hq, Hkv, D, pstore.page_size)
-        p_qo, p_kvp, p_idx, p_last = dev_idx(pcall)
-        p_ws = torch.empty(bia.bia_prefill_workspace_size(pdesc, pcall.qo_indptr,
-                                                          pcall.kv_indptr,
-                                                          pcall.kv_last_page_len),
-                           dtype=torch.uint8, device=dev)
-        p_out = torch.empty_like(pcall.q)
-        p_lse = torch.empty(pcall.total_q, Hq, dtype=torch.float32, device=dev)
+        prefill = prefill_call(pstore, pcall)
         flops = prefill_flops(pcall, D, Hq)
-
-        def prefill():
-            bia.bia_prefill_paged(pdesc, pcall.q, pstore.k_cache, pstore.v_cache, p_qo, p_kvp,
-                                  p_idx, p_last, pcall.qo_indptr, pcall.kv_indptr,
-                                  pcall.kv_last_page_len, p_ws, p_out, p_lse, stream=stream)
     if do_d:
         dstore = wl.cfg4_decode(dev, args.decode_batch)
         dcall = wl.whole_prefill(dstore)
         Hq, Hkv, D = dstore.num_qo_heads, dstore.num_kv_heads, dstore.head_dim
-        ddesc = bia.make_desc(Hq, Hkv, D, dstore.page_size)
-        _, d_kvp, d_idx, d_last = dev_idx(dcall)
-        d_ws = torch.empty(bia.bia_decode_workspace_size(ddesc, dcall.kv_indptr,
-                                                         dcall.kv_last_page_len),
-                           dtype=torch.uint8, device=dev)
-        d_out = torch.empty_like(dcall.q)
-        d_lse = torch.empty(dcall.total_q, Hq, dtype=torch.float32, device=dev)
+        decode = decode_call(dstore, dcall)
         dbytes = kv_bytes(dcall, Hkv, D)
 
-        def decode():
-            bia.bia_decode_paged(ddesc, dcall.q, dstore.k_cache, dstore.v_cache, d_kvp, d_idx,
-                                 d_last, dcall.kv_indptr, dcall.kv_last_page_len, d_ws, d_out,
-                                 d_lse, stream=stream)
-
-    # ---- device-timed loop
+    # ---- device-timed loop: a step = the prefill call then the decode call
     n = args.warmup + args.steps
     e_step = [(ev(), ev(), ev()) for _ in range(n)]
     e_pk = [(ev(), ev()) for _ in range(n)]
@@ -628,132 +699,191 @@ def main():
         step(i)
     bia.bia_set_profile_events(None, None)
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
     launches0 = bia.bia_launch_count()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(0) as clocks:
         torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
         t_wall0 = time.perf_counter()
         for i in range(args.warmup, n):
             step(i)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
-        if dist:
-            dist.barrier()
     bia.bia_set_profile_events(None, None)
     launches = bia.bia_launch_count() - launches0
     timed = range(args.warmup, n)
-    pre_ms = [e_step[i][0].elapsed_time(e_step[i][1]) for i in timed]
-    dec_ms = [e_step[i][1].elapsed_time(e_step[i][2]) for i in timed]
-    pk_ms = [e_pk[i][0].elapsed_time(e_pk[i][1]) if prefill else 0.0 for i in timed]
-    dk_ms = [e_dk[i][0].elapsed_time(e_dk[i][1]) if decode else 0.0 for i in timed]
     K = args.steps
-    local = [sum(pre_ms) / 1000.0, sum(dec_ms) / 1000.0, sum(pk_ms) / 1000.0,
-             sum(dk_ms) / 1000.0]
-    flops_rate, (pre_s, dec_s, pk_s, dk_s) = aggregate_over_ranks(local, flops, K, dist, dev)
-    value = flops_rate / 1e12 if prefill else None
-    dec_gbs = world * dbytes * K / dec_s / 1e9 if decode else None
+    pre_s = sum(e_step[i][0].elapsed_time(e_step[i][1]) for i in timed) / 1000.0
+    dec_s = sum(e_step[i][1].elapsed_time(e_step[i][2]) for i in timed) / 1000.0
+    pk_s = sum(e_pk[i][0].elapsed_time(e_pk[i][1]) for i in timed) / 1000.0 if prefill else 0.0
+    dk_s = sum(e_dk[i][0].elapsed_time(e_dk[i][1]) for i in timed) / 1000.0 if decode else 0.0
+    value = flops * K / pre_s / 1e12 if prefill else None
+    dec_gbs = dbytes * K / dec_s / 1e9 if decode else None
     pk_avg, dk_avg = pk_s / K, dk_s / K
 
     # ---- the timed outputs are finite (parity is the test suite's job)
     if prefill:
-        assert torch.isfinite(p_out.float()).all()
+        assert torch.isfinite(prefill.out.float()).all()
     if decode:
-        assert torch.isfinite(d_out.float()).all()
-
-    # ---- end to end through host buffers (prefill call, the headline metric)
-    e2e = None
-    if prefill and not args.no_e2e:
-        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-        hq, hk, hv = pin(pcall.q), pin(pstore.k_cache), pin(pstore.v_cache)
-        h_idx = [pin(t) for t in (pcall.qo_indptr, pcall.kv_indptr, pcall.kv_indices,
-                                  pcall.kv_last_page_len)]
-        h_out, h_lse = torch.empty_like(hq).pin_memory(), torch.empty_like(p_lse.cpu()).pin_memory()
-        dq, dk, dv = torch.empty_like(pcall.q), torch.empty_like(pstore.k_cache), \
-            torch.empty_like(pstore.v_cache)
-        d_idx4 = [torch.empty_like(t, device=dev) for t in h_idx]
-        h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv] + h_idx)
-        d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
-
-        def e2e_step():
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            for dst, src in zip(d_idx4, h_idx):
-                dst.copy_(src, non_blocking=True)
-            bia.bia_prefill_paged(pdesc, dq, dk, dv, *d_idx4, pcall.qo_indptr, pcall.kv_indptr,
-                                  pcall.kv_last_page_len, p_ws, p_out, p_lse, stream=stream)
-            h_out.copy_(p_out, non_blocking=True)
-            h_lse.copy_(p_lse, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        ke = min(K, 20)
-        a, b = ev(), ev()
-        a.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_s = torch.tensor([a.elapsed_time(b) / 1000.0], dtype=torch.float64, device=dev)
-        if dist:
-            dist.all_reduce(e2e_s, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * flops * ke / e2e_s.item() / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": ke, "scope": "prefill call incl. H2D of q/K/V/index arrays from pinned "
-                                     "host memory and D2H of out+lse"}
+        assert torch.isfinite(decode.out.float()).all()
 
     peaks, peak_kind = load_peaks()
-    pk_achieved = flops / pk_avg / 1e12 if prefill else 0.0
-    dk_achieved = dbytes / dk_avg / 1e9 if decode else 0.0
     # counters are keyed by the kernel's own translation unit
     pre_src = ["invariant_paged_attention_gb300/csrc/prefill.cu"]
     dec_src = ["invariant_paged_attention_gb300/csrc/decode.cu"]
-    roofline = {"bound": "tensor", "kernel": "prefill_kernel<128>", "achieved": pk_achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": pk_achieved / peaks["bf16_tflops"],
-                "frac_of_sustained": pk_achieved / peaks["bf16_tflops_sustained"],
-                "peak_source": f"bf16 dense burst, of {peak_kind}",
-                "algorithmic_flops_per_launch": flops, "kernel_ms": pk_avg * 1e3,
-                "traffic": traffic_from_profiles("prefill_kernel<128>", pre_src, flops)}
-    dec_roof = {"bound": "hbm", "kernel": "decode_kernel<128,4,false>", "achieved": dk_achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dk_achieved / peaks["hbm_gbs"],
-                "peak_source": f"HBM copy, of {peak_kind}", "kv_bytes_per_launch": dbytes,
-                "kernel_ms": dk_avg * 1e3,
-                "traffic": traffic_from_profiles("decode_kernel<128,4,false>", dec_src, dbytes)
-                if decode else None}
+    roofline = roofline_of("tensor", flops, pk_avg * 1e3, peaks, peak_kind, "prefill_kernel<128>",
+                           traffic_from_profiles("prefill_kernel<128>", pre_src, flops)) \
+        if prefill else None
+    dec_roof = roofline_of("hbm", dbytes, dk_avg * 1e3, peaks, peak_kind,
+                           "decode_kernel<128,4,false>",
+                           traffic_from_profiles("decode_kernel<128,4,false>", dec_src, dbytes)) \
+        if decode else None
+
+    # ---- end to end through host buffers: each step copies its inputs from
+    # pinned host memory (q, the K/V caches, the index arrays), makes the
+    # call, and copies out + lse back
+    def pin(t):
+        h = torch.empty(tuple(t.shape), dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    def host_available_bytes():
+        try:
+            with open("/proc/meminfo") as fh:
+                for ln in fh:
+                    if ln.startswith("MemAvailable:"):
+                        return int(ln.split()[1]) * 1024
+        except OSError:
+            pass
+        return 0
+
+    def e2e_leg(fn, store, call, is_decode, work, unit_scale, steps):
+        cache_bytes = 2 * store.k_cache.numel() * store.k_cache.element_size()
+        if host_available_bytes() < 4 * cache_bytes:
+            return {"value": None, "skipped": "pinned host copies of the caches would take "
+                                              "more than a quarter of the free host memory"}
+        hq, hk, hv = pin(call.q), pin(store.k_cache), pin(store.v_cache)
+        names = (call.kv_indptr, call.kv_indices, call.kv_last_page_len) if is_decode else \
+            (call.qo_indptr, call.kv_indptr, call.kv_indices, call.kv_last_page_len)
+        h_idx = [pin(t) for t in names]
+        h_out = torch.empty(tuple(hq.shape), dtype=hq.dtype, pin_memory=True)
+        h_lse = torch.empty(tuple(fn.lse.shape), dtype=torch.float32, pin_memory=True)
+        dq, dk, dv = torch.empty_like(call.q), torch.empty_like(store.k_cache), \
+            torch.empty_like(store.v_cache)
+        d_idx = [torch.empty_like(t, device=dev) for t in h_idx]
+        h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv] + h_idx)
+        d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+        def one():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            for dst, src in zip(d_idx, h_idx):
+                dst.copy_(src, non_blocking=True)
+            fn(dq, dk, dv, d_idx)
+            h_out.copy_(fn.out, non_blocking=True)
+            h_lse.copy_(fn.lse, non_blocking=True)
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+        torch.cuda.synchronize()
+        secs = a.elapsed_time(b) / 1000.0
+        del dq, dk, dv, d_idx, hk, hv
+        return {"value": work * steps / secs / unit_scale, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+    e2e = dec_e2e = None
+    if not args.no_e2e:
+        if prefill:
+            e2e = e2e_leg(prefill, pstore, pcall, False, flops, 1e12, min(K, 20))
+            e2e.update(unit="TFLOP/s", scope="prefill call incl. H2D of q/K/V/index arrays "
+                                              "from pinned host memory and D2H of out+lse")
+        if decode:
+            dec_e2e = e2e_leg(decode, dstore, dcall, True, dbytes, 1e9, min(K, 5))
+            dec_e2e.update(unit="GB/s", scope="decode call incl. H2D of q/K/V/index arrays "
+                                               "from pinned host memory and D2H of out+lse")
+
+    # ---- every other workload, each call timed alone (L2 flushed before each)
+    configs = {}
+    if args.only == "both" and not args.no_configs:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        leg = Leg(bia, stream, flush)
+        cs, cw = max(3, min(args.steps, 10)), 3
+
+        def put(name, kind, work, cm, km, launches, kernel, desc_txt, extra=None):
+            unit, scale = ("TFLOP/s", 1e9) if kind == "tensor" else ("GB/s", 1e6)
+            rec = {"workload": desc_txt, "value": work / cm / scale, "unit": unit,
+                   "call_ms": cm, "gpu_launches_per_call": launches,
+                   "roofline": roofline_of(kind, work, km, peaks, peak_kind, kernel) if km else None}
+            rec.update(extra or {})
+            configs[name] = rec
+
+        st = wl.cfg3_prefix(dev)
+        whole = wl.whole_prefill(st)
+        fl = prefill_flops(whole, 128, 32)
+        f = prefill_call(st, whole)
+        cm, km, nl = leg.run([f], cs, cw)
+        put("cfg3_unchunked", "tensor", fl, cm, km, nl, "prefill_kernel<128>",
+            "prefixes 1/511/2048/4097 + 16384 new tokens, one extend call, page 1")
+        fns = [prefill_call(st, c) for c in wl.chunked_calls(st, 256)]
+        cm, _, nl = leg.run(fns, cs, cw)
+        put("cfg3_chunks256", "tensor", fl, cm, None, nl, "prefill_kernel<128>",
+            "the same extend as 64 calls of 256-token chunks (on the 32-token grid)",
+            {"note": "call_ms covers all 64 chunk calls"})
+        del st, whole, f, fns
+        pst, dst = wl.cfg5_mixed(dev)
+        pc, dc = wl.whole_prefill(pst), wl.whole_prefill(dst)
+        f = prefill_call(pst, pc)
+        cm, km, nl = leg.run([f], cs, cw)
+        put("cfg5_prefill_call", "tensor", prefill_flops(pc, 128, 32), cm, km, nl,
+            "prefill_kernel<128> + streamed tiles",
+            "one 4096-token chunk (prefix 4096) + 64 one-token extends (ctx U[1024,32768]), "
+            "page 16", {"kv_bytes": kv_bytes(pc, 8, 128)})
+        f = decode_call(dst, dc)
+        cm, km, nl = leg.run([f], cs, cw)
+        put("cfg5_decodes", "hbm", kv_bytes(dc, 8, 128), cm, km, nl,
+            "decode_kernel<128,4,false>", "32 decodes at 131072 context, page 16")
+        del pst, dst, pc, dc, f
+        for B in (1, 8, 64):
+            st = wl.cfg4_decode(dev, B)
+            c = wl.whole_prefill(st)
+            f = decode_call(st, c)
+            cm, km, nl = leg.run([f], cs, cw)
+            put(f"cfg4_b{B}", "hbm", kv_bytes(c, 8, 128), cm, km, nl,
+                "decode_kernel<128,4,false>", f"{B} decodes, ctx U[1024,32768], page 1")
+            del st, c, f
+        del flush
+        torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and prefill and not args.no_cpu_baseline:
+    if prefill and not args.no_cpu_baseline:
         v, cores, desc, _ = oracle_sample_rate(pcall, args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
 
-    if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-                "steps": K, "warmup": args.warmup,
-                "ms_per_step": (pre_s + dec_s) * 1000.0 / K, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic (seeded N(0,1) bf16, random page tables)",
-                "config": {"workload": WORKLOAD if args.only == "both" and args.decode_batch == 256
-                           else f"{args.only} only (decode batch {args.decode_batch})",
-                           "prefill_tokens": pcall.total_q if prefill else 0,
-                           "prefill_algorithmic_flops": flops,
-                           "decode_requests": dcall.batch if decode else 0,
-                           "decode_kv_bytes": dbytes, "parallelism": f"replicas x{world}",
-                           "l2": "inputs larger than L2 (prefill q+K+V ~0.43 GB, decode K+V "
-                                 "~17.7 GB streamed between prefill steps)"},
-                "decode": {"value": dec_gbs, "unit": "GB/s",
-                           "ms_per_call": dec_s * 1000.0 / K, "roofline": dec_roof},
-                "prefill_ms_per_call": pre_s * 1000.0 / K,
-                "roofline": roofline if prefill else dec_roof, "e2e": e2e, "cpu_baseline": cpu,
-                "clocks": clocks.summary(), "gpu_launches": int(launches) * world,
-                "wall_s_timed": t_wall}
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": K, "warmup": args.warmup,
+            "ms_per_step": (pre_s + dec_s) * 1000.0 / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, random page tables)",
+            "config": {"workload": WORKLOAD if args.only == "both" and args.decode_batch == 256
+                       else f"{args.only} only (decode batch {args.decode_batch})",
+                       "prefill_tokens": pcall.total_q if prefill else 0,
+                       "prefill_algorithmic_flops": flops,
+                       "decode_requests": dcall.batch if decode else 0,
+                       "decode_kv_bytes": dbytes, "parallelism": "one GPU",
+                       "l2": "main step: inputs larger than L2 (prefill q+K+V ~0.43 GB, decode "
+                             "K+V ~17.2 GB streamed between prefill steps); configs: L2 flushed "
+                             "(256 MiB write) before every timed call"},
+            "decode": {"value": dec_gbs, "unit": "GB/s",
+                       "ms_per_call": dec_s * 1000.0 / K, "roofline": dec_roof, "e2e": dec_e2e},
+            "prefill_ms_per_call": pre_s * 1000.0 / K,
+            "roofline": roofline if prefill else dec_roof, "e2e": e2e, "cpu_baseline": cpu,
+            "configs": configs, "clocks": clocks.summary(), "gpu_launches": int(launches),
+            "wall_s_timed": t_wall}
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

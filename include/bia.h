@@ -37,7 +37,12 @@
  * h / (num_qo_heads / num_kv_heads).  sm_scale <= 0 selects 1/sqrt(head_dim).
  *
  * Ownership: the caller owns every buffer and the stream; the library never
- * allocates device memory and never synchronises the stream.  The *_host
+ * allocates device memory and never synchronises the stream.  Every device
+ * pointer must be device memory (cudaMalloc or a pool carved from it) of the
+ * current device: the prefill kernels multicast each gathered K/V row into
+ * the CTAs of a thread-block cluster, which this library does for this GPU's
+ * own memory only, so a host, managed or peer-mapped pointer is refused with
+ * BIA_ERR_INVALID_ARG (bia_last_error names it) before anything is enqueued.  The *_host
  * arrays are read synchronously during the call (to validate and to size the
  * launch) and must equal their device copies.  All work is enqueued on
  * `stream` (a cudaStream_t; NULL = legacy default stream) on the current
@@ -49,7 +54,10 @@
  * Errors: every entry point returns BIA_OK or a negative bia_status and never
  * aborts.  Host-side checks run before anything is enqueued.  A page index
  * outside [0, num_pages) is caught on the device: the row is read as zeros and
- * bit 0 of the workspace status word is set (bia_read_status).
+ * bit 0 of the workspace status word is set (bia_read_status).  The device
+ * planner also checks the device index arrays (lengths, page counts, and the
+ * bounds of a bounded call); when a check fails it computes nothing, leaves
+ * out and lse unwritten and sets bit 1 of the status word.
  *
  * Alignment: q, out, the caches and every bf16 row buffer start on a 16-byte
  * boundary; int32 and fp32 arrays on 4 bytes, int64 arrays on 8; a call
@@ -172,6 +180,71 @@ BIA_API size_t bia_decode_workspace_size(const bia_attn_desc *desc, const int32_
                                  const int32_t *kv_last_page_len_host, int32_t batch,
                                  int32_t split_size);
 
+/*
+ * Bounded calls: a prefill or decode whose launch is sized from upper bounds
+ * instead of the host mirrors, so that one captured CUDA graph replays across
+ * serving steps while the lengths and page tables in the device arrays change
+ * (each decode step adds a key; each chunk of a chunked prefill adds its
+ * tokens).  The pages keep split-KV under CUDA graphs only by turning it off
+ * during capture and replay ("sglang PR #10417 [POC] Support deterministic
+ * inference", Modifications); here the fixed split tiles stay: the device
+ * planner lays out the units the actual lengths need in the same order as the
+ * exact call and retires the rest, so a bounded call's out and lse bits equal
+ * those of bia_prefill_paged / bia_decode_paged on the same inputs.  Nothing
+ * is read from the host: the index arrays are read only on the device, and a
+ * request beyond the bounds (or malformed arrays) sets status bit 1 and
+ * computes nothing.  The price is a launch sized for the bounds (retired
+ * units exit at once) and a workspace sized for them.
+ */
+typedef struct bia_bounds {
+    int32_t max_q_len;   /* q tokens of any one request (prefill; decode ignores it) */
+    int32_t max_kv_len;  /* keys of any one request, >= 1 for decode */
+    int64_t max_total_q; /* q tokens of the whole call (prefill; decode ignores it):
+                            q, out and lse must hold this many token rows */
+} bia_bounds;
+
+/*
+ * bia_prefill_paged sized from `bounds` (see above): request b's lengths come
+ * from qo_indptr / kv_indptr / kv_last_page_len on the device only, within
+ * max_q_len, max_kv_len and qo_indptr[batch] <= max_total_q; kv_indices must
+ * hold kv_indptr[batch] entries.  The workspace is
+ * bia_prefill_bounded_workspace_size's; everything else as for
+ * bia_prefill_paged.
+ */
+BIA_API int bia_prefill_paged_bounded(const bia_attn_desc *desc, const bia_bounds *bounds,
+                                      const void *q, const void *k_cache, const void *v_cache,
+                                      int64_t num_pages, const int32_t *qo_indptr,
+                                      const int32_t *kv_indptr, const int32_t *kv_indices,
+                                      const int32_t *kv_last_page_len, int32_t batch,
+                                      int32_t causal, int32_t split_size, void *workspace,
+                                      size_t workspace_bytes, void *out, float *lse,
+                                      void *stream);
+
+/* Workspace bytes of every bounded prefill of `batch` requests within
+ * `bounds` (0 on invalid input). */
+BIA_API size_t bia_prefill_bounded_workspace_size(const bia_attn_desc *desc,
+                                                  const bia_bounds *bounds, int32_t batch,
+                                                  int32_t causal, int32_t split_size);
+
+/*
+ * bia_decode_paged sized from `bounds` (max_kv_len; see above): every request
+ * owns 1 .. max_kv_len keys, read from the device arrays only.  The workspace
+ * is bia_decode_bounded_workspace_size's.
+ */
+BIA_API int bia_decode_paged_bounded(const bia_attn_desc *desc, const bia_bounds *bounds,
+                                     const void *q, const void *k_cache, const void *v_cache,
+                                     int64_t num_pages, const int32_t *kv_indptr,
+                                     const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                                     int32_t batch, int32_t split_size, void *workspace,
+                                     size_t workspace_bytes, void *out, float *lse,
+                                     void *stream);
+
+/* Workspace bytes of every bounded decode of `batch` requests within
+ * `bounds` (0 on invalid input). */
+BIA_API size_t bia_decode_bounded_workspace_size(const bia_attn_desc *desc,
+                                                 const bia_bounds *bounds, int32_t batch,
+                                                 int32_t split_size);
+
 /* Size of the library-owned scratch array behind bia_decode_paged_noalloc. */
 #define BIA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -189,11 +262,16 @@ BIA_API size_t bia_decode_workspace_size(const bia_attn_desc *desc, const int32_
  * until the process exits; a call whose bia_decode_workspace_size exceeds it
  * returns BIA_ERR_WORKSPACE_TOO_SMALL without enqueuing anything.  Nothing is
  * allocated (no cudaMalloc / cudaFree).  The first call on each device looks
- * up the array's device address with that device current; make that first
- * call before any stream capture.  All calls share the one array, which keeps
- * the previous call's contents (every call rewrites what it reads), so calls
- * whose work overlaps on the GPU - different streams, or different host
- * threads - race and must be serialised by the caller.
+ * up the array's device address with that device current and keeps it for
+ * the life of the process; make that first call before any stream capture,
+ * and do not call this entry point after a cudaDeviceReset (the kept address
+ * would be stale).  All calls share the one array, which keeps the previous
+ * call's contents (every call rewrites what it reads), so calls whose work
+ * overlaps on the GPU - different streams, or different host threads - race
+ * and must be serialised by the caller.  The device status word (bad page
+ * indices, a failed device plan) lives in that array, whose address the
+ * caller never sees, so it cannot be read with bia_read_status: a caller that
+ * needs those checks uses bia_decode_paged.
  */
 BIA_API int bia_decode_paged_noalloc(const bia_attn_desc *desc, const void *q, const void *k_cache,
                              const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
@@ -338,15 +416,17 @@ BIA_API int32_t bia_q_tile_tokens(int32_t gqa_group);
 /* Static text for a bia_status value. */
 BIA_API const char *bia_status_string(int status);
 
-/* Detail of the last BIA_ERR_CUDA returned in the calling thread (the CUDA
- * or driver call that failed and its error); empty if none. */
+/* Detail of the last failure in the calling thread: the CUDA or driver call
+ * behind a BIA_ERR_CUDA and its error, or the pointer a residency check
+ * refused; empty if none. */
 BIA_API const char *bia_last_error(void);
 
 /*
  * Copies the device status word of the last call that used `workspace`
- * (bit 0: a page index was out of range; bit 1: the device plan disagreed with
- * the host-sized launch; bit 2: a device wait timed out) into *status_out.
- * Synchronises `stream`.
+ * (bit 0: a page index was out of range; bit 1: the device index arrays
+ * disagreed with the host-sized launch, broke a rule of the call or exceeded
+ * the bounds of a bounded call, and nothing was computed; bit 2: a device wait
+ * timed out) into *status_out.  Synchronises `stream`.
  */
 BIA_API int bia_read_status(const void *workspace, int32_t *status_out, void *stream);
 

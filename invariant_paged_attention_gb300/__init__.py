@@ -39,7 +39,9 @@ EXPORTS = ("bia_prefill_paged", "bia_prefill_workspace_size", "bia_decode_paged"
            "bia_launch_count", "bia_last_error", "bia_decode_paged_noalloc",
            "bia_append_paged_kv", "bia_prefill_paged_mask", "bia_mla_decode_paged",
            "bia_mla_decode_workspace_size", "bia_mla_prefill_paged",
-           "bia_mla_prefill_workspace_size")
+           "bia_mla_prefill_workspace_size", "bia_prefill_paged_bounded",
+           "bia_prefill_bounded_workspace_size", "bia_decode_paged_bounded",
+           "bia_decode_bounded_workspace_size")
 
 
 class BiaError(RuntimeError):
@@ -66,6 +68,11 @@ class MlaDesc(ctypes.Structure):
 
 
 MLA_CKV_DIM, MLA_KPE_DIM = 512, 64
+
+
+class Bounds(ctypes.Structure):
+    _fields_ = [("max_q_len", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
+                ("max_total_q", ctypes.c_int64)]
 
 
 def load(path: str = LIB_PATH):
@@ -123,6 +130,17 @@ def load(path: str = LIB_PATH):
     lib.bia_mla_prefill_paged.restype = ctypes.c_int
     lib.bia_mla_prefill_workspace_size.argtypes = [mp, vp, vp, vp, i32, i32]
     lib.bia_mla_prefill_workspace_size.restype = sz
+    bp = ctypes.POINTER(Bounds)
+    lib.bia_prefill_paged_bounded.argtypes = [dp, bp, vp, vp, vp, i64, vp, vp, vp, vp, i32, i32,
+                                              i32, vp, sz, vp, vp, vp]
+    lib.bia_prefill_paged_bounded.restype = ctypes.c_int
+    lib.bia_prefill_bounded_workspace_size.argtypes = [dp, bp, i32, i32, i32]
+    lib.bia_prefill_bounded_workspace_size.restype = sz
+    lib.bia_decode_paged_bounded.argtypes = [dp, bp, vp, vp, vp, i64, vp, vp, vp, i32, i32, vp,
+                                             sz, vp, vp, vp]
+    lib.bia_decode_paged_bounded.restype = ctypes.c_int
+    lib.bia_decode_bounded_workspace_size.argtypes = [dp, bp, i32, i32]
+    lib.bia_decode_bounded_workspace_size.restype = sz
     _lib = lib
     return lib
 
@@ -314,6 +332,70 @@ def bia_decode_paged(desc, q, k_cache, v_cache, kv_indptr, kv_indices, kv_last_p
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
     if rc != BIA_OK:
         raise BiaError(rc, "bia_decode_paged")
+
+
+def make_bounds(max_q_len=1, max_kv_len=1, max_total_q=0) -> Bounds:
+    return Bounds(int(max_q_len), int(max_kv_len), int(max_total_q))
+
+
+def bia_prefill_bounded_workspace_size(desc, bounds, batch, causal=True, split_size=0) -> int:
+    return int(load().bia_prefill_bounded_workspace_size(ctypes.byref(desc), ctypes.byref(bounds),
+                                                         int(batch), int(bool(causal)),
+                                                         int(split_size)))
+
+
+def bia_decode_bounded_workspace_size(desc, bounds, batch, split_size=0) -> int:
+    return int(load().bia_decode_bounded_workspace_size(ctypes.byref(desc), ctypes.byref(bounds),
+                                                        int(batch), int(split_size)))
+
+
+def bia_prefill_paged_bounded(desc, bounds, q, k_cache, v_cache, qo_indptr, kv_indptr,
+                              kv_indices, kv_last_page_len, workspace, out, lse=None,
+                              causal=True, split_size=0, stream=None):
+    """bia_prefill_paged sized from `bounds` (a Bounds): the index arrays are
+    read on the device only, so a captured call replays while they change.
+    q / out / lse hold bounds.max_total_q token rows."""
+    ts = _check_types(("q", q, BF16), ("k_cache", k_cache, BF16), ("v_cache", v_cache, BF16),
+                      ("qo_indptr", qo_indptr, I32), ("kv_indptr", kv_indptr, I32),
+                      ("kv_indices", kv_indices, I32), ("kv_last_page_len", kv_last_page_len, I32),
+                      ("workspace", workspace, None), ("out", out, BF16), ("lse", lse, F32, True))
+    _check_caches(k_cache, v_cache)
+    _check_rows(q, out, lse)
+    if q.shape[0] < bounds.max_total_q:
+        raise ValueError(f"q holds {q.shape[0]} token rows, bounds.max_total_q is "
+                         f"{bounds.max_total_q}")
+    _check_cuda(ts, stream)
+    rc = load().bia_prefill_paged_bounded(
+        ctypes.byref(desc), ctypes.byref(bounds), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        k_cache.shape[0], _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices),
+        _ptr(kv_last_page_len), qo_indptr.numel() - 1, int(bool(causal)), int(split_size),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_prefill_paged_bounded")
+
+
+def bia_decode_paged_bounded(desc, bounds, q, k_cache, v_cache, kv_indptr, kv_indices,
+                             kv_last_page_len, workspace, out, lse=None, split_size=0,
+                             stream=None):
+    """bia_decode_paged sized from `bounds` (max_kv_len): the index arrays are
+    read on the device only, so a captured decode replays step after step."""
+    ts = _check_types(("q", q, BF16), ("k_cache", k_cache, BF16), ("v_cache", v_cache, BF16),
+                      ("kv_indptr", kv_indptr, I32), ("kv_indices", kv_indices, I32),
+                      ("kv_last_page_len", kv_last_page_len, I32), ("workspace", workspace, None),
+                      ("out", out, BF16), ("lse", lse, F32, True))
+    _check_caches(k_cache, v_cache)
+    _check_rows(q, out, lse)
+    if q.shape[0] != kv_indptr.numel() - 1:
+        raise ValueError(f"q holds {q.shape[0]} rows for {kv_indptr.numel() - 1} requests")
+    _check_cuda(ts, stream)
+    rc = load().bia_decode_paged_bounded(
+        ctypes.byref(desc), ctypes.byref(bounds), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        k_cache.shape[0], _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len),
+        kv_indptr.numel() - 1, int(split_size), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
+    if rc != BIA_OK:
+        raise BiaError(rc, "bia_decode_paged_bounded")
 
 
 BIA_DECODE_NOALLOC_SCRATCH_BYTES = 64 << 20

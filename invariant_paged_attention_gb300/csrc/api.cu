@@ -4,8 +4,10 @@
 // synchronisation (except bia_read_status, which exists to synchronise).
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 
 #include <cudaTypedefs.h>
 
@@ -45,6 +47,39 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 // kernels read int32 / fp32 words, int64 offsets and 16-byte vectors).
 bool misaligned(const void *p, uintptr_t align) {
   return (reinterpret_cast<uintptr_t>(p) & (align - 1)) != 0;
+}
+
+// Every non-null pointer of `ptrs` must be device memory of the current
+// device.  The kernels read and write these addresses directly, and the
+// prefill kernels' TMA gathers multicast each loaded row into every CTA of
+// their cluster, which is defined here for this GPU's own memory only; a host
+// buffer (pinned or not), managed memory or another GPU's peer-mapped buffer
+// is refused with BIA_ERR_INVALID_ARG before anything is enqueued.
+struct NamedPtr {
+  const char *name;
+  const void *p;
+};
+int check_resident(std::initializer_list<NamedPtr> ptrs) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  for (const NamedPtr &x : ptrs) {
+    if (!x.p) continue;
+    cudaPointerAttributes at{};
+    e = cudaPointerGetAttributes(&at, x.p);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError(); // not sticky: keep it from reaching a later launch check
+      return cuda_fail("cudaPointerGetAttributes", e);
+    }
+    if (at.type != cudaMemoryTypeDevice || at.device != dev) {
+      std::snprintf(g_last_error, sizeof g_last_error,
+                    "%s is not device memory of the current device %d (memory type %d, "
+                    "device %d)",
+                    x.name, dev, static_cast<int>(at.type), at.device);
+      return BIA_ERR_INVALID_ARG;
+    }
+  }
+  return BIA_OK;
 }
 
 int log2i(int x) {
@@ -201,19 +236,66 @@ int check_mask(const MaskArgs &m, const int32_t *qo, const int32_t *kvp, const i
   return BIA_OK;
 }
 
+// Plan sizes that cover every call of `batch` requests within `bd` (a
+// bounded call): the largest group, unit, streamed-unit and partial-row
+// counts any such call can need, so that one launch configuration (and one
+// captured CUDA graph) serves all of them.  The device planner fills the
+// units the actual lengths need and retires the rest.
+int bounded_plan(const bia_bounds *bd, int32_t batch, int32_t causal, int32_t split,
+                 int tile_tokens, int tiles_per_unit, int ctas, int stream, bool decode,
+                 HostPlan *hp) {
+  if (!bd || batch <= 0) return BIA_ERR_INVALID_ARG;
+  if (split <= 0 || split % bia::kKvBlock != 0) return BIA_ERR_UNSUPPORTED;
+  const int64_t max_kv = bd->max_kv_len;
+  int64_t max_q = decode ? 1 : bd->max_q_len;
+  const int64_t total_q = decode ? batch : bd->max_total_q;
+  if (max_kv < (decode ? 1 : 0) || max_q < 0 || total_q < 0) return BIA_ERR_INVALID_ARG;
+  if (max_kv > INT32_MAX / 2 || max_q > INT32_MAX / 2) return BIA_ERR_UNSUPPORTED;
+  if (causal && max_q > max_kv) max_q = max_kv; // a causal request has q_len <= kv_len
+  if (max_q > total_q) max_q = total_q;
+  const int64_t s_max = max_kv > 0 ? (max_kv + split - 1) / split : 1;
+  const int64_t gt = bia::group_tiles(tiles_per_unit, ctas);
+  const int64_t tiles_max = (max_q + tile_tokens - 1) / tile_tokens;
+  HostPlan p;
+  // sum over requests of ceil(q_len / (tile_tokens * gt)) is at most
+  // batch + total_q / (tile_tokens * gt)
+  p.n_groups = std::min<int64_t>(static_cast<int64_t>(batch) * ((tiles_max + gt - 1) / gt),
+                                 batch + total_q / (tile_tokens * gt));
+  p.n_units = p.n_groups * ctas * s_max;
+  p.n_sunits = (stream && tile_tokens > 1) ? std::min<int64_t>(batch, total_q) * s_max : 0;
+  p.part_rows = s_max > 1 ? std::min<int64_t>(static_cast<int64_t>(batch) * max_q, total_q) *
+                                s_max
+                          : 0;
+  p.total_q = total_q;
+  if (p.n_units > INT32_MAX) return BIA_ERR_UNSUPPORTED;
+  *hp = p;
+  return BIA_OK;
+}
+
+// Optional parts of an attention call.
+struct CallOpts {
+  const MaskArgs *mask = nullptr;
+  const bia_bounds *bounds = nullptr; // bounded call: plan sized from bounds, no host mirrors
+  bool ws_static = false;             // the workspace is the library's own scratch array
+  size_t *need = nullptr;             // check only: report the workspace bytes and return
+};
+
 int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const void *k_cache,
                   const void *v_cache, int64_t num_pages, const int32_t *qo_indptr,
                   const int32_t *kv_indptr, const int32_t *kv_indices,
                   const int32_t *kv_last_page_len, const int32_t *qo_host,
                   const int32_t *kvp_host, const int32_t *last_host, int32_t batch,
                   int32_t causal, int32_t split, void *workspace, size_t workspace_bytes,
-                  void *out, float *lse, void *stream, const MaskArgs *mask = nullptr) {
+                  void *out, float *lse, void *stream, const CallOpts &opt = CallOpts{}) {
+  const MaskArgs *mask = opt.mask;
+  const bool bounded = opt.bounds != nullptr;
   int rc = check_desc(desc);
   if (rc != BIA_OK) return rc;
   if (!q || !k_cache || !v_cache || !kv_indptr || !kv_indices || !kv_last_page_len || !out ||
-      !workspace || num_pages <= 0)
+      num_pages <= 0)
     return BIA_ERR_INVALID_ARG;
-  if (!decode && (!qo_indptr || !qo_host)) return BIA_ERR_INVALID_ARG;
+  if (!opt.need && !workspace) return BIA_ERR_INVALID_ARG;
+  if (!decode && (!qo_indptr || (!bounded && !qo_host))) return BIA_ERR_INVALID_ARG;
   if (misaligned(workspace, 256)) return BIA_ERR_INVALID_ARG;
   if (misaligned(q, 16) || misaligned(k_cache, 16) || misaligned(v_cache, 16) ||
       misaligned(out, 16) || misaligned(lse, 4) || misaligned(qo_indptr, 4) ||
@@ -227,21 +309,41 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   const int stream_tail = decode ? 0 : 1;
   if (decode) causal = 1;
   HostPlan hp;
-  rc = host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal, split,
-                 tile_tokens, tiles_per_unit, ctas, stream_tail, &hp);
+  rc = bounded ? bounded_plan(opt.bounds, batch, causal, split, tile_tokens, tiles_per_unit,
+                              ctas, stream_tail, decode, &hp)
+               : host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, causal,
+                           split, tile_tokens, tiles_per_unit, ctas, stream_tail, &hp);
   if (rc != BIA_OK) return rc;
+  if (decode && hp.n_units * desc->num_kv_heads > INT32_MAX) return BIA_ERR_UNSUPPORTED;
   if (mask) {
     rc = check_mask(*mask, qo_host, kvp_host, last_host, batch, desc->page_size);
     if (rc != BIA_OK) return rc;
   }
   const WsLayout w = bia::make_layout(batch, hp.n_groups, hp.n_units, hp.n_sunits,
                                       hp.part_rows, desc->num_qo_heads, desc->head_dim);
+  if (opt.need) {
+    *opt.need = w.total;
+    return BIA_OK;
+  }
   if (workspace_bytes < w.total) return BIA_ERR_WORKSPACE_TOO_SMALL;
   if (hp.total_q == 0) return BIA_OK;
 
   const int64_t q_rows = hp.total_q * desc->num_qo_heads;
   const int64_t kv_rows = num_pages * desc->page_size * desc->num_kv_heads;
   if (!decode && (q_rows >= INT32_MAX || kv_rows >= INT32_MAX)) return BIA_ERR_UNSUPPORTED;
+  rc = check_resident({{"q", q},
+                       {"k_cache", k_cache},
+                       {"v_cache", v_cache},
+                       {"out", out},
+                       {"lse", lse},
+                       {"qo_indptr", qo_indptr},
+                       {"kv_indptr", kv_indptr},
+                       {"kv_indices", kv_indices},
+                       {"kv_last_page_len", kv_last_page_len},
+                       {"mask", mask ? mask->bits : nullptr},
+                       {"mask_indptr", mask ? mask->indptr : nullptr},
+                       {"workspace", opt.ws_static ? nullptr : workspace}});
+  if (rc != BIA_OK) return rc;
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -258,6 +360,12 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   pa.causal = causal;
   pa.split = split;
   pa.stream = stream_tail;
+  pa.bounded = bounded ? 1 : 0;
+  if (bounded) {
+    pa.max_q_len = decode ? 1 : opt.bounds->max_q_len;
+    pa.max_kv_len = opt.bounds->max_kv_len;
+    pa.max_total_q = hp.total_q;
+  }
   pa.n_groups_expected = hp.n_groups;
   pa.n_units_expected = hp.n_units;
   pa.n_sunits_expected = hp.n_sunits;
@@ -345,18 +453,21 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
 
 size_t workspace_size(bool decode, const bia_attn_desc *desc, const int32_t *qo_host,
                       const int32_t *kvp_host, const int32_t *last_host, int32_t batch,
-                      int32_t causal, int32_t split) {
+                      int32_t causal, int32_t split, const bia_bounds *bounds = nullptr) {
   if (check_desc(desc) != BIA_OK) return 0;
-  if (!decode && !qo_host) return 0;
+  if (!decode && !qo_host && !bounds) return 0;
   if (split == 0) split = decode ? BIA_DECODE_SPLIT : BIA_PREFILL_SPLIT;
   const int G = desc->num_qo_heads / desc->num_kv_heads;
   const int tile_tokens = decode ? 1 : bia::kTileRows / G;
   const int tiles_per_unit = decode ? 1 : bia::prefill_tiles_per_unit(desc->head_dim);
   const int ctas = decode ? 1 : bia::kPrefillClusterCtas;
   HostPlan hp;
-  if (host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch, decode ? 1 : causal,
-                split, tile_tokens, tiles_per_unit, ctas, decode ? 0 : 1, &hp) != BIA_OK)
-    return 0;
+  const int rc = bounds ? bounded_plan(bounds, batch, decode ? 1 : causal, split, tile_tokens,
+                                       tiles_per_unit, ctas, decode ? 0 : 1, decode, &hp)
+                        : host_plan(desc, decode ? nullptr : qo_host, kvp_host, last_host, batch,
+                                    decode ? 1 : causal, split, tile_tokens, tiles_per_unit, ctas,
+                                    decode ? 0 : 1, &hp);
+  if (rc != BIA_OK) return 0;
   return bia::make_layout(batch, hp.n_groups, hp.n_units, hp.n_sunits, hp.part_rows,
                           desc->num_qo_heads, desc->head_dim)
       .total;
@@ -389,10 +500,12 @@ int bia_prefill_paged_mask(const bia_attn_desc *desc, const void *q, const void 
                            const int64_t *mask_indptr_host, void *workspace,
                            size_t workspace_bytes, void *out, float *lse, void *stream) {
   const MaskArgs m{mask, mask_bytes, mask_indptr, mask_indptr_host};
+  CallOpts opt;
+  opt.mask = &m;
   return run_attention(false, desc, q, k_cache, v_cache, num_pages, qo_indptr, kv_indptr,
                        kv_indices, kv_last_page_len, qo_indptr_host, kv_indptr_host,
                        kv_last_page_len_host, batch, causal ? 1 : 0, split_size, workspace,
-                       workspace_bytes, out, lse, stream, &m);
+                       workspace_bytes, out, lse, stream, opt);
 }
 
 size_t bia_prefill_workspace_size(const bia_attn_desc *desc, const int32_t *qo_indptr_host,
@@ -422,6 +535,49 @@ size_t bia_decode_workspace_size(const bia_attn_desc *desc, const int32_t *kv_in
                         split_size);
 }
 
+int bia_prefill_paged_bounded(const bia_attn_desc *desc, const bia_bounds *bounds,
+                              const void *q, const void *k_cache, const void *v_cache,
+                              int64_t num_pages, const int32_t *qo_indptr,
+                              const int32_t *kv_indptr, const int32_t *kv_indices,
+                              const int32_t *kv_last_page_len, int32_t batch, int32_t causal,
+                              int32_t split_size, void *workspace, size_t workspace_bytes,
+                              void *out, float *lse, void *stream) {
+  if (!bounds) return BIA_ERR_INVALID_ARG;
+  CallOpts opt;
+  opt.bounds = bounds;
+  return run_attention(false, desc, q, k_cache, v_cache, num_pages, qo_indptr, kv_indptr,
+                       kv_indices, kv_last_page_len, nullptr, nullptr, nullptr, batch,
+                       causal ? 1 : 0, split_size, workspace, workspace_bytes, out, lse, stream,
+                       opt);
+}
+
+size_t bia_prefill_bounded_workspace_size(const bia_attn_desc *desc, const bia_bounds *bounds,
+                                          int32_t batch, int32_t causal, int32_t split_size) {
+  if (!bounds) return 0;
+  return workspace_size(false, desc, nullptr, nullptr, nullptr, batch, causal ? 1 : 0,
+                        split_size, bounds);
+}
+
+int bia_decode_paged_bounded(const bia_attn_desc *desc, const bia_bounds *bounds, const void *q,
+                             const void *k_cache, const void *v_cache, int64_t num_pages,
+                             const int32_t *kv_indptr, const int32_t *kv_indices,
+                             const int32_t *kv_last_page_len, int32_t batch, int32_t split_size,
+                             void *workspace, size_t workspace_bytes, void *out, float *lse,
+                             void *stream) {
+  if (!bounds) return BIA_ERR_INVALID_ARG;
+  CallOpts opt;
+  opt.bounds = bounds;
+  return run_attention(true, desc, q, k_cache, v_cache, num_pages, nullptr, kv_indptr,
+                       kv_indices, kv_last_page_len, nullptr, nullptr, nullptr, batch, 1,
+                       split_size, workspace, workspace_bytes, out, lse, stream, opt);
+}
+
+size_t bia_decode_bounded_workspace_size(const bia_attn_desc *desc, const bia_bounds *bounds,
+                                         int32_t batch, int32_t split_size) {
+  if (!bounds) return 0;
+  return workspace_size(true, desc, nullptr, nullptr, nullptr, batch, 1, split_size, bounds);
+}
+
 int bia_merge_states(const float *v, const float *s, const int32_t *num_states, int64_t n,
                      int32_t num_states_max, int32_t num_heads, int32_t head_dim, void *out,
                      float *out_lse, void *stream) {
@@ -432,6 +588,12 @@ int bia_merge_states(const float *v, const float *s, const int32_t *num_states, 
   if (misaligned(v, 16) || misaligned(out, 8) || misaligned(s, 4) || misaligned(out_lse, 4) ||
       misaligned(num_states, 4))
     return BIA_ERR_INVALID_ARG;
+  const int rc = check_resident({{"v", v},
+                                 {"s", s},
+                                 {"num_states", num_states},
+                                 {"out", out},
+                                 {"out_lse", out_lse}});
+  if (rc != BIA_OK) return rc;
   cudaError_t e = bia::launch_merge_states(v, s, num_states, n, num_states_max, num_heads,
                                            head_dim, static_cast<uint16_t *>(out), out_lse,
                                            static_cast<cudaStream_t>(stream));
@@ -464,19 +626,33 @@ int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void
   }
   const int64_t total_new = append_indptr_host[batch];
   if (misaligned(status, 4)) return BIA_ERR_INVALID_ARG;
+  if (total_new > 0) {
+    if (!k_new || !v_new || !k_cache || !v_cache || !append_indptr || !kv_indptr ||
+        !kv_indices || !kv_last_page_len || num_pages <= 0)
+      return BIA_ERR_INVALID_ARG;
+    if (misaligned(k_new, 16) || misaligned(v_new, 16) || misaligned(k_cache, 16) ||
+        misaligned(v_cache, 16) || misaligned(append_indptr, 4) || misaligned(kv_indptr, 4) ||
+        misaligned(kv_indices, 4) || misaligned(kv_last_page_len, 4))
+      return BIA_ERR_INVALID_ARG;
+  }
+  if (total_new > 0 || status) {
+    rc = check_resident({{"status", status},
+                         {"k_new", total_new > 0 ? k_new : nullptr},
+                         {"v_new", total_new > 0 ? v_new : nullptr},
+                         {"k_cache", total_new > 0 ? k_cache : nullptr},
+                         {"v_cache", total_new > 0 ? v_cache : nullptr},
+                         {"append_indptr", total_new > 0 ? append_indptr : nullptr},
+                         {"kv_indptr", total_new > 0 ? kv_indptr : nullptr},
+                         {"kv_indices", total_new > 0 ? kv_indices : nullptr},
+                         {"kv_last_page_len", total_new > 0 ? kv_last_page_len : nullptr}});
+    if (rc != BIA_OK) return rc;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (status) {
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
     if (e != cudaSuccess) return cuda_fail("status reset", e);
   }
   if (total_new == 0) return BIA_OK;
-  if (!k_new || !v_new || !k_cache || !v_cache || !append_indptr || !kv_indptr || !kv_indices ||
-      !kv_last_page_len || num_pages <= 0)
-    return BIA_ERR_INVALID_ARG;
-  if (misaligned(k_new, 16) || misaligned(v_new, 16) || misaligned(k_cache, 16) ||
-      misaligned(v_cache, 16) || misaligned(append_indptr, 4) || misaligned(kv_indptr, 4) ||
-      misaligned(kv_indices, 4) || misaligned(kv_last_page_len, 4))
-    return BIA_ERR_INVALID_ARG;
   bia::AppendArgs a{};
   a.k_new = static_cast<const uint16_t *>(k_new);
   a.v_new = static_cast<const uint16_t *>(v_new);
@@ -498,6 +674,41 @@ int bia_append_paged_kv(const bia_attn_desc *desc, const void *k_new, const void
   __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
   return BIA_OK;
 }
+
+} // extern "C"
+
+namespace bia {
+
+int decode_check(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                 const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
+                 const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                 const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                 int32_t batch, int32_t split_size, void *out, float *lse, size_t *need) {
+  CallOpts opt;
+  opt.need = need;
+  return run_attention(true, desc, q, k_cache, v_cache, num_pages, nullptr, kv_indptr,
+                       kv_indices, kv_last_page_len, nullptr, kv_indptr_host,
+                       kv_last_page_len_host, batch, 1, split_size, nullptr, 0, out, lse,
+                       nullptr, opt);
+}
+
+int decode_on_scratch(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                      const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
+                      const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                      const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                      int32_t batch, int32_t split_size, void *scratch, size_t scratch_bytes,
+                      void *out, float *lse, void *stream) {
+  CallOpts opt;
+  opt.ws_static = true;
+  return run_attention(true, desc, q, k_cache, v_cache, num_pages, nullptr, kv_indptr,
+                       kv_indices, kv_last_page_len, nullptr, kv_indptr_host,
+                       kv_last_page_len_host, batch, 1, split_size, scratch, scratch_bytes, out,
+                       lse, stream, opt);
+}
+
+} // namespace bia
+
+extern "C" {
 
 namespace {
 // Multi-head latent attention: validation and plan sizes as for the GQA
@@ -553,6 +764,18 @@ int run_mla(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
   const int64_t q_rows = hp.total_q * desc->num_heads;
   const int64_t kv_rows = num_pages * desc->page_size;
   if (q_rows >= INT32_MAX || kv_rows >= INT32_MAX) return BIA_ERR_UNSUPPORTED;
+  rc = check_resident({{"q_nope", q_nope},
+                       {"q_pe", q_pe},
+                       {"ckv_cache", ckv_cache},
+                       {"kpe_cache", kpe_cache},
+                       {"out", out},
+                       {"lse", lse},
+                       {"qo_indptr", extend ? qo_indptr : nullptr},
+                       {"kv_indptr", kv_indptr},
+                       {"kv_indices", kv_indices},
+                       {"kv_last_page_len", kv_last_page_len},
+                       {"workspace", workspace}});
+  if (rc != BIA_OK) return rc;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -699,6 +922,8 @@ const char *bia_status_string(int status) {
 
 int bia_read_status(const void *workspace, int32_t *status_out, void *stream) {
   if (!workspace || !status_out) return BIA_ERR_INVALID_ARG;
+  const int rc = check_resident({{"workspace", workspace}});
+  if (rc != BIA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(status_out, workspace, sizeof(int32_t),
                                   cudaMemcpyDeviceToHost, st);

@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "../../include/bia.h"
+
 #include <cuda.h> // CUtensorMap (a plain 128-byte struct; no driver-library link needed)
 #include <cuda_runtime.h>
 
@@ -152,6 +154,13 @@ struct PlanArgs {
   const int32_t *kv_last_page_len;
   int32_t batch, page_size, tile_tokens, tiles_per_unit, ctas, causal, split;
   int32_t stream; // 1: single-token tail tiles become streamed units (prefill)
+  // 0: the launch was sized from the host mirrors and the device plan must
+  // match it exactly; 1: it was sized from bounds (the *_expected counts are
+  // capacities), every request must lie within them, and the units the
+  // actual lengths do not need are retired
+  int32_t bounded;
+  int32_t max_q_len, max_kv_len; // per-request bounds (bounded calls)
+  int64_t max_total_q;            // q tokens of the call (bounded calls)
   int64_t n_groups_expected, n_units_expected, n_sunits_expected, part_rows_expected;
   int32_t *status;
   ReqInfo *reqs;
@@ -206,6 +215,23 @@ struct AppendArgs {
   int32_t batch, Hkv, D, page_size;
   int32_t *status; // may be NULL
 };
+
+// The decode of bia_decode_paged split in two for the static-scratch entry
+// point: decode_check runs every host-side check of the call and reports the
+// workspace bytes it needs (*need), enqueuing nothing; decode_on_scratch runs
+// the call on the library's own scratch array (its residency is not checked:
+// the address comes from the runtime for the current device).
+int decode_check(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                 const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
+                 const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                 const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                 int32_t batch, int32_t split_size, void *out, float *lse, size_t *need);
+int decode_on_scratch(const bia_attn_desc *desc, const void *q, const void *k_cache,
+                      const void *v_cache, int64_t num_pages, const int32_t *kv_indptr,
+                      const int32_t *kv_indices, const int32_t *kv_last_page_len,
+                      const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
+                      int32_t batch, int32_t split_size, void *scratch, size_t scratch_bytes,
+                      void *out, float *lse, void *stream);
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);

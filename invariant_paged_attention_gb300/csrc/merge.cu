@@ -72,9 +72,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t token = blockIdx.x;
   if (token >= a.total_rows) return;
+  // a plan that failed its checks computed nothing: leave out unwritten
+  if (a.status[0] & kStatusPlanMismatch) return;
   const int b = a.qo_indptr ? owner(a.qo_indptr, a.batch, token) : static_cast<int>(token);
   const ReqInfo r = a.reqs[b];
   const int32_t t = static_cast<int32_t>(token - r.q_start);
+  if (t >= r.q_len) return; // past the call's last token (a launch sized from bounds)
   const int32_t tile = t / a.tile_tokens;
   const int32_t n_tile = tile_splits(r.q_len, r.kv_len, tile, a.tile_tokens, a.causal, a.split);
   if (n_tile <= 1 || r.rowbase < 0) return;

@@ -12,9 +12,13 @@
 //   D. per group: its units (the request's last groups first: they carry the
 //      most keys); for each split, one unit per CTA of a cluster
 //
-// The host sizes the launch from its mirrors of the same arrays; when the
-// device arrays disagree, every unit is disabled and a status bit is set
-// instead of reading or writing out of bounds.
+// The host sizes the launch either from its mirrors of the same arrays (the
+// device plan must then match it exactly) or, for a bounded call, from
+// per-request bounds (the launch then has room for every call within them:
+// the units the actual lengths need come first and the rest are retired).
+// Each request is also checked here (lengths, page counts, the bounds): when
+// any check fails or the plan does not fit the launch, every unit is retired
+// and a status bit is set instead of reading or writing out of bounds.
 #include "bia_internal.h"
 
 namespace bia {
@@ -23,17 +27,30 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-__device__ inline void request_geometry(const PlanArgs &a, int b, int32_t &q_start,
+// Request b's q range and key count; false (and zero lengths) when its index
+// arrays break a rule of the call: negative lengths, a last-page length
+// outside 1..page_size, more than 2^30 keys, q_len > kv_len when causal, no
+// key in a decode, or (bounded calls) lengths beyond the bounds.
+__device__ inline bool request_geometry(const PlanArgs &a, int b, int32_t &q_start,
                                         int32_t &q_len, int32_t &kv_len) {
+  int64_t ql;
   if (a.qo_indptr) {
     q_start = a.qo_indptr[b];
-    q_len = a.qo_indptr[b + 1] - q_start;
+    ql = static_cast<int64_t>(a.qo_indptr[b + 1]) - q_start;
   } else {
     q_start = b;
-    q_len = 1;
+    ql = 1;
   }
-  const int32_t pages = a.kv_indptr[b + 1] - a.kv_indptr[b];
-  kv_len = pages > 0 ? (pages - 1) * a.page_size + a.kv_last_page_len[b] : 0;
+  const int64_t pages = static_cast<int64_t>(a.kv_indptr[b + 1]) - a.kv_indptr[b];
+  const int32_t last = a.kv_last_page_len[b];
+  const int64_t kl = pages > 0 ? (pages - 1) * a.page_size + last : 0;
+  bool ok = ql >= 0 && pages >= 0 && (pages == 0 || (last >= 1 && last <= a.page_size)) &&
+            kl <= INT32_MAX / 2 && ql <= INT32_MAX / 2 && (!a.causal || ql <= kl) &&
+            (a.qo_indptr || kl > 0);
+  if (a.bounded) ok = ok && ql <= a.max_q_len && kl <= a.max_kv_len;
+  q_len = ok ? static_cast<int32_t>(ql) : 0;
+  kv_len = ok ? static_cast<int32_t>(kl) : 0;
+  return ok;
 }
 
 // Exclusive scan of one value per thread across the block; returns the
@@ -90,9 +107,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   const int per = (a.batch + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
   int64_t my_groups = 0, my_rows = 0, my_sunits = 0;
+  bool bad = false;
+  if (tid == 0) {
+    bad = a.kv_indptr[0] < 0 || (a.qo_indptr && a.qo_indptr[0] != 0);
+    if (a.bounded && a.qo_indptr) bad = bad || a.qo_indptr[a.batch] > a.max_total_q;
+  }
   for (int b = lo; b < hi; ++b) {
     int32_t q_start, q_len, kv_len;
-    request_geometry(a, b, q_start, q_len, kv_len);
+    bad = !request_geometry(a, b, q_start, q_len, kv_len) || bad;
     const int32_t tiles = (q_len + a.tile_tokens - 1) / a.tile_tokens;
     const int32_t nsp = tiles > 0 ? tile_splits(q_len, kv_len, tiles - 1, a.tile_tokens,
                                                 a.causal, a.split) : 1;
@@ -100,15 +122,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (nsp > 1) my_rows += static_cast<int64_t>(q_len) * nsp;
     if (streamed_tail(q_len, a.tile_tokens, a.stream)) my_sunits += nsp;
   }
+  const bool any_bad = __syncthreads_or(bad) != 0;
   int64_t total_groups, total_rows, total_sunits;
   int64_t group = block_exclusive_scan<int64_t>(my_groups, s_scan, &total_groups);
   int64_t row = block_exclusive_scan<int64_t>(my_rows, s_scan, &total_rows);
   int64_t sunit = block_exclusive_scan<int64_t>(my_sunits, s_scan, &total_sunits);
   // every thread sees the same totals: the streamed units below are written
   // only when they fit the host-sized list
-  const bool sizes_ok = total_groups == a.n_groups_expected &&
-                        total_rows == a.part_rows_expected &&
-                        total_sunits == a.n_sunits_expected;
+  const bool sizes_ok =
+      !any_bad && (a.bounded ? total_groups <= a.n_groups_expected &&
+                                   total_rows <= a.part_rows_expected &&
+                                   total_sunits <= a.n_sunits_expected
+                             : total_groups == a.n_groups_expected &&
+                                   total_rows == a.part_rows_expected &&
+                                   total_sunits == a.n_sunits_expected);
   if (tid == 0) {
     s_ok = sizes_ok;
     if (s_ok) a.group_off[a.batch] = static_cast<int32_t>(total_groups);
@@ -140,7 +167,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     row += rows;
   }
   __syncthreads();
-  const int32_t n_groups = static_cast<int32_t>(a.n_groups_expected);
+  // the groups this call has (equal to the host's count unless bounded)
+  const int32_t n_groups = sizes_ok ? static_cast<int32_t>(total_groups) : 0;
 
   // ---- B: split count of every group (reversed within its request)
   if (s_ok) {
@@ -168,7 +196,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (s_ok && g < n_groups) a.group_cnt[g] = static_cast<int32_t>(carry + excl);
     carry += chunk_total;
   }
-  if (tid == 0 && s_ok && carry != a.n_units_expected) s_ok = 0;
+  if (tid == 0 && s_ok && (a.bounded ? carry > a.n_units_expected : carry != a.n_units_expected))
+    s_ok = 0;
   __syncthreads();
   if (!s_ok) {
     if (tid == 0) atomicOr(a.status, kStatusPlanMismatch);
@@ -197,6 +226,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.units[u++] = Unit{b, tc, s, max(0, min(a.tiles_per_unit, tiles - tc))};
       }
   }
+  // a bounded launch has room for more units than these lengths need: the
+  // rest are retired (whole clusters, as the live count is a multiple of ctas)
+  for (int64_t i = carry + tid; i < a.n_units_expected; i += kPlanThreads)
+    a.units[i] = Unit{-1, 0, 0, 0};
+  for (int64_t i = total_sunits + tid; i < a.n_sunits_expected; i += kPlanThreads)
+    a.sunits[i] = Unit{-1, 0, 0, 0};
 }
 
 } // namespace

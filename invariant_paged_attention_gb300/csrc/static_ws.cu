@@ -29,7 +29,8 @@ void *g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 // Device address of the array on the current device, looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached for the life of the process
+// (a cudaDeviceReset would leave the cached address stale).
 int scratch_address(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return BIA_ERR_CUDA;
@@ -54,21 +55,20 @@ int bia_decode_paged_noalloc(const bia_attn_desc *desc, const void *q, const voi
                              const int32_t *kv_indptr_host, const int32_t *kv_last_page_len_host,
                              int32_t batch, int32_t split_size, void *out, float *lse,
                              void *stream) {
-  const size_t need = bia_decode_workspace_size(desc, kv_indptr_host, kv_last_page_len_host,
-                                                batch, split_size);
-  if (need == 0) {
-    // invalid arguments: let the regular entry point report which status
-    return bia_decode_paged(desc, q, k_cache, v_cache, num_pages, kv_indptr, kv_indices,
-                            kv_last_page_len, kv_indptr_host, kv_last_page_len_host, batch,
-                            split_size, nullptr, 0, out, lse, stream);
-  }
+  // every host-side check of bia_decode_paged first, with its status codes;
+  // nothing touches the GPU until the call is known to be valid and to fit
+  size_t need = 0;
+  int rc = bia::decode_check(desc, q, k_cache, v_cache, num_pages, kv_indptr, kv_indices,
+                             kv_last_page_len, kv_indptr_host, kv_last_page_len_host, batch,
+                             split_size, out, lse, &need);
+  if (rc != BIA_OK) return rc;
   if (need > kStaticScratchBytes) return BIA_ERR_WORKSPACE_TOO_SMALL;
   void *ws = nullptr;
-  const int rc = scratch_address(&ws);
+  rc = scratch_address(&ws);
   if (rc != BIA_OK) return rc;
-  return bia_decode_paged(desc, q, k_cache, v_cache, num_pages, kv_indptr, kv_indices,
-                          kv_last_page_len, kv_indptr_host, kv_last_page_len_host, batch,
-                          split_size, ws, kStaticScratchBytes, out, lse, stream);
+  return bia::decode_on_scratch(desc, q, k_cache, v_cache, num_pages, kv_indptr, kv_indices,
+                                kv_last_page_len, kv_indptr_host, kv_last_page_len_host, batch,
+                                split_size, ws, kStaticScratchBytes, out, lse, stream);
 }
 
 } // extern "C"

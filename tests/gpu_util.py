@@ -96,11 +96,12 @@ def compact(call: wl.Call, part_ids) -> wl.Call:
 
 
 def check_rows(call: wl.Call, out, lse, part_ids=None, tokens_per_part=None, seed=0,
-               causal=True, sm_scale=None, threads=None):
+               causal=True, sm_scale=None, threads=None, tokens=None):
     """Compares GPU rows with the oracle.  part_ids: which parts (default all);
     tokens_per_part: None = every token, else a seeded sample of that many
-    tokens per part, always including the first and last q tile.  Returns
-    (max_abs, mean_abs, rows_checked)."""
+    tokens per part, always including the first and last q tile; tokens: an
+    explicit list of in-part token indices instead (those inside each part).
+    Returns (max_abs, mean_abs, rows_checked)."""
     part_ids = list(range(call.batch)) if part_ids is None else list(part_ids)
     sub = compact(call, part_ids)
     st = call.store
@@ -113,7 +114,11 @@ def check_rows(call: wl.Call, out, lse, part_ids=None, tokens_per_part=None, see
         if n == 0:
             continue
         toks = np.arange(n)
-        if tokens_per_part is not None and n > tokens_per_part:
+        if tokens is not None:
+            toks = np.array(sorted(t for t in set(tokens) if 0 <= t < n), dtype=np.int64)
+            if toks.size == 0:
+                continue
+        elif tokens_per_part is not None and n > tokens_per_part:
             edge = np.concatenate([np.arange(min(T, n)), np.arange(max(0, n - T), n)])
             pick = rng.choice(n, size=tokens_per_part, replace=False)
             toks = np.unique(np.concatenate([edge, pick]))

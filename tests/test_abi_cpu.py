@@ -257,3 +257,106 @@ def test_binding_constants_match_the_header(bia):
         "BIA_ERR_UNSUPPORTED": bia.BIA_ERR_UNSUPPORTED,
         "BIA_ERR_WORKSPACE_TOO_SMALL": bia.BIA_ERR_WORKSPACE_TOO_SMALL,
         "BIA_ERR_CUDA": bia.BIA_ERR_CUDA}
+
+
+def test_noalloc_decode_reports_the_regular_status_codes(bia):
+    """The static-scratch decode runs every host-side check of the regular
+    decode first, so a bad split or a request without keys gets the same
+    status, before anything touches a GPU."""
+    lib = bia.load()
+    p = ctypes.c_void_p
+    d = bia.make_desc(**QWEN)
+    kvp = torch.tensor([0, 10], dtype=torch.int32)
+    last = torch.tensor([1], dtype=torch.int32)
+
+    def call(split, kvp=kvp):
+        return lib.bia_decode_paged_noalloc(ctypes.byref(d), p(FAKE), p(FAKE), p(FAKE), 1 << 20,
+                                            p(FAKE), p(FAKE), p(FAKE), p(kvp.data_ptr()),
+                                            p(last.data_ptr()), 1, split, p(FAKE), None, None)
+    assert call(100) == bia.BIA_ERR_UNSUPPORTED  # not a multiple of 128
+    assert call(0, torch.tensor([0, 0], dtype=torch.int32)) == bia.BIA_ERR_INVALID_ARG
+
+
+def test_host_pointers_are_refused_before_any_launch(bia):
+    """A call whose every argument is valid but whose buffers live in host
+    memory returns an error and launches nothing (without a GPU the residency
+    check itself cannot run and the call fails with BIA_ERR_CUDA)."""
+    lib = bia.load()
+    p = ctypes.c_void_p
+    d = bia.make_desc(32, 8, 128, 16)
+    kvp = torch.tensor([0, 2], dtype=torch.int32)
+    last = torch.tensor([5], dtype=torch.int32)
+    idx = torch.tensor([0, 1], dtype=torch.int32)
+    k = torch.zeros(2, 16, 8, 128, dtype=torch.bfloat16)
+    q = torch.zeros(1, 32, 128, dtype=torch.bfloat16)
+    out = torch.zeros_like(q)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8)
+    wsp = (ws.data_ptr() + 255) // 256 * 256
+    before = lib.bia_launch_count()
+    rc = lib.bia_decode_paged(ctypes.byref(d), p(q.data_ptr()), p(k.data_ptr()), p(k.data_ptr()),
+                              2, p(kvp.data_ptr()), p(idx.data_ptr()), p(last.data_ptr()),
+                              p(kvp.data_ptr()), p(last.data_ptr()), 1, 0, p(wsp), 1 << 19,
+                              p(out.data_ptr()), None, None)
+    assert rc in (bia.BIA_ERR_INVALID_ARG, bia.BIA_ERR_CUDA)
+    assert lib.bia_launch_count() == before
+
+
+def test_bounded_workspace_covers_every_call_within_the_bounds(bia):
+    """A bounded call's workspace holds the plan of any call within its
+    bounds: never smaller than the exact size of a random such call."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for Hq, Hkv, D, P in [(32, 8, 128, 1), (32, 8, 128, 16), (16, 8, 256, 1), (8, 8, 64, 4)]:
+        d = bia.make_desc(Hq, Hkv, D, P)
+        for _ in range(20):
+            B = int(rng.integers(1, 9))
+            max_q, max_kv = int(rng.integers(1, 3000)), int(rng.integers(1, 20000))
+            max_kv = max(max_kv, max_q)
+            total = int(rng.integers(max_q, B * max_q + 1))
+            bd = bia.make_bounds(max_q, max_kv, total)
+            cap = bia.bia_prefill_bounded_workspace_size(d, bd, B)
+            dcap = bia.bia_decode_bounded_workspace_size(d, bd, B)
+            assert cap > 0 and dcap > 0
+            # a random call inside the bounds
+            kv = rng.integers(1, max_kv + 1, B)
+            q = np.minimum(rng.integers(0, max_q + 1, B), kv)
+            while q.sum() > total:
+                q[int(np.argmax(q))] -= 1
+            pages = -(-kv // P)
+            qo = torch.tensor(np.concatenate([[0], np.cumsum(q)]), dtype=torch.int32)
+            kvp = torch.tensor(np.concatenate([[0], np.cumsum(pages)]), dtype=torch.int32)
+            last = torch.tensor(kv - (pages - 1) * P, dtype=torch.int32)
+            assert bia.bia_prefill_workspace_size(d, qo, kvp, last) <= cap
+            assert bia.bia_decode_workspace_size(d, kvp, last) <= dcap
+
+
+def test_bounded_calls_reject_bad_arguments_on_the_host(bia):
+    lib = bia.load()
+    p = ctypes.c_void_p
+    d = bia.make_desc(**QWEN)
+
+    def prefill(bounds, split=0, ws_bytes=1 << 30, batch=2):
+        return lib.bia_prefill_paged_bounded(
+            ctypes.byref(d), None if bounds is None else ctypes.byref(bounds), p(FAKE), p(FAKE),
+            p(FAKE), 1 << 20, p(FAKE), p(FAKE), p(FAKE), p(FAKE), batch, 1, split, p(FAKE),
+            ws_bytes, p(FAKE), None, None)
+
+    def decode(bounds, split=0):
+        return lib.bia_decode_paged_bounded(
+            ctypes.byref(d), None if bounds is None else ctypes.byref(bounds), p(FAKE), p(FAKE),
+            p(FAKE), 1 << 20, p(FAKE), p(FAKE), p(FAKE), 4, split, p(FAKE), 1 << 30, p(FAKE),
+            None, None)
+    inv = bia.BIA_ERR_INVALID_ARG
+    assert prefill(None) == inv
+    assert prefill(bia.make_bounds(100, -1, 200)) == inv
+    assert prefill(bia.make_bounds(-1, 100, 200)) == inv
+    assert prefill(bia.make_bounds(100, 1000, 200), batch=0) == inv
+    assert prefill(bia.make_bounds(100, 1000, 200), split=100) == bia.BIA_ERR_UNSUPPORTED
+    assert prefill(bia.make_bounds(100, 1 << 30, 200)) == bia.BIA_ERR_UNSUPPORTED
+    assert prefill(bia.make_bounds(100, 1000, 200), ws_bytes=64) == \
+        bia.BIA_ERR_WORKSPACE_TOO_SMALL
+    assert decode(None) == inv
+    assert decode(bia.make_bounds(1, 0, 0)) == inv  # a decode request owns at least one key
+    assert decode(bia.make_bounds(1, 1000, 0), split=100) == bia.BIA_ERR_UNSUPPORTED
+    assert bia.bia_decode_bounded_workspace_size(d, bia.make_bounds(1, 0, 0), 4) == 0
+    assert bia.bia_prefill_bounded_workspace_size(d, bia.make_bounds(1, 10, -1), 4) == 0

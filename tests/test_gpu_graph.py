@@ -1,13 +1,17 @@
 """The entry points inside a CUDA graph: nothing in a call copies host data to
 the device (the plan is built by a device kernel from the device index
 arrays), so a prefill + decode step captured once replays with new q and K/V
-values and gives the same bits as eager calls on those values."""
+values and gives the same bits as eager calls on those values, and matches
+the oracle on them.  Replays across steps whose lengths change are covered
+by the bounded calls' tests."""
+import dataclasses
+
 import pytest
 import torch
 
 import invariant_paged_attention_gb300 as bia
 import workloads as wl
-from tests.gpu_util import same_bits
+from tests.gpu_util import check_rows, same_bits
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -80,6 +84,9 @@ def test_captured_prefill_and_decode_replay_bit_identically():
         assert same_bits(g[0], e_pout) and same_bits(g[1], e_plse)
         assert same_bits(g[2], e_dout) and same_bits(g[3], e_dlse)
         assert torch.isfinite(g[0].float()).all()
+        # and the replayed values themselves against the oracle
+        check_rows(dataclasses.replace(pcall, q=pq.clone()), g[0], g[1])
+        check_rows(dataclasses.replace(dcall, q=dq.clone()), g[2], g[3])
 
 
 def test_captured_append_extend_and_mla_replay_bit_identically():

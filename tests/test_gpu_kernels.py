@@ -60,6 +60,11 @@ DECODE_CASES = [
     (16, 8, 128, 4, [999, 4100]),
     (64, 8, 128, 1, [2500, 10]),
     (4, 1, 64, 1, [3000, 64]),
+    # the larger pages the header allows
+    (32, 8, 128, 32, [5000, 33, 1]),
+    (32, 8, 128, 64, [2049, 700]),
+    (32, 8, 128, 256, [9000, 1, 300]),
+    (16, 8, 256, 128, [4100, 77]),
 ]
 
 
@@ -132,6 +137,12 @@ PREFILL_CASES = [
     (64, 8, 128, 2, [(3, 200)], True, 256),
     (32, 8, 128, 1, [(0, 100), (50, 70)], False, 0),
     (32, 8, 128, 1, [(200, 0), (0, 40), (0, 0), (9, 3)], True, 0),
+    # the larger pages the header allows
+    (32, 8, 128, 32, [(0, 500), (100, 40)], True, 0),
+    (32, 8, 128, 64, [(4000, 300), (0, 65)], True, 0),
+    (32, 8, 128, 256, [(0, 700), (300, 33)], True, 1024),
+    (16, 8, 256, 64, [(0, 400), (70, 129)], True, 0),
+    (8, 8, 64, 128, [(5, 250)], False, 0),
 ]
 
 

@@ -49,7 +49,7 @@ def decode_store(ctxs, H, P, seed):
                        P, DEV, layout_seed=seed)
 
 
-@pytest.mark.parametrize("H,P", [(16, 1), (8, 16), (128, 1)])
+@pytest.mark.parametrize("H,P", [(16, 1), (8, 16), (128, 1), (16, 64), (32, 256)])
 def test_mla_decode_matches_oracle(H, P):
     st = decode_store([1, 100, 2048, 2049, 9000], H, P, seed=3000 + H + P)
     call = wl.mla_call(st, [(i, 0, 1) for i in range(len(st.seqs))])
