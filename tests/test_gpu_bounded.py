@@ -23,7 +23,7 @@ def bounded_prefill(call, bounds, q=None, split=0):
     desc = desc_of(st)
     ws = torch.empty(bia.bia_prefill_bounded_workspace_size(desc, bounds, call.batch, True, split),
                      dtype=torch.uint8, device=DEV)
-    rows = bounds.max_total_q
+    rows = max(bounds.max_total_q, call.total_q)  # room for a call beyond its bounds
     qb = torch.zeros((rows, st.num_qo_heads, st.head_dim), dtype=torch.bfloat16, device=DEV)
     qb[:call.total_q] = call.q if q is None else q
     out = torch.full_like(qb, float("nan"))
