@@ -218,6 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // shared-memory descriptors of the operand tiles, built once: a K step
+      // only advances the start-address field (16-byte units; every address
+      // is below 2^18, so the 14-bit field never carries), which keeps the
+      // issue of each MMA to a few instructions
+      const uint64_t dQ0 = desc_sw128(sQ(0), 16, 1024), dQ1 = desc_sw128(sQ(1), 16, 1024);
+      const uint64_t dK0 = desc_sw128(sK(0), 16, 1024), dK1 = desc_sw128(sK(1), 16, 1024);
+      const uint64_t dV0 = desc_sw128(sV(0), kAtom, 1024), dV1 = desc_sw128(sV(1), kAtom, 1024);
       bool ok = !any_tile || mbar_wait(bar(L::kQFull), 0, a.status);
       auto wait_k = [&](int j) {
         ok = ok && mbar_wait(bar(L::kKFull + (j & 1)), (j >> 1) & 1, a.status);
@@ -226,11 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       auto issue_s = [&](int t, int j) {
         if (!ok) return;
         const int st = j & 1;
+        const uint64_t dq = t ? dQ1 : dQ0, dk = st ? dK1 : dK0;
+        const uint32_t ts = tS(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kAtom + (kk & 3) * 32;
-          mma_bf16_ss(tS(t), desc_sw128(sQ(t) + koff, 16, 1024),
-                      desc_sw128(sK(st) + koff, 16, 1024), kIdescS, kk > 0);
+          const uint32_t koff = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(ts, dq + koff, dk + koff, kIdescS, kk > 0);
         }
         mma_commit(bar(L::kSFull + t));
       };
@@ -239,10 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         ok = ok && mbar_wait(bar(L::kPFull + t), j & 1, a.status);
         if (!ok) return;
         tc_fence_after();
+        const uint64_t dv = st ? dV1 : dV0;
+        const uint32_t to = tO(t), ts = tS(t);
 #pragma unroll
         for (int kk = 0; kk < kKvBlock / 16; ++kk)
-          mma_bf16_ts(tO(t), tS(t) + kk * 8, desc_sw128(sV(st) + kk * 2048, kAtom, 1024),
-                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(to, ts + kk * 8, dv + ((kk * 2048) >> 4), kIdescPV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
         if (j == nb - 1) mma_commit(bar(L::kODone + t));
       };
       // A stage is released (to every CTA) only when a later block will
