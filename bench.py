@@ -460,6 +460,12 @@ def sweep_d256(wl, dev, time_calls, prefill_fn, decode_fn, emit, prefill_flops, 
     emit("head_dim 256 prefill (cfg2 lengths, 16q/8kv, page 1)", "prefill",
          prefill_flops(c, 256, 16), cm, km)
     del st, c
+    st = wl.wide_prefill(dev, page_size=16)
+    c = wl.whole_prefill(st)
+    cm, km = time_calls([prefill_fn(st, c)])
+    emit("head_dim 256 prefill (cfg2 lengths, 16q/8kv, page 16)", "prefill",
+         prefill_flops(c, 256, 16), cm, km)
+    del st, c
     st = wl.wide_decode(dev, 64)
     c = wl.whole_prefill(st)
     cm, km = time_calls([decode_fn(st, c)])

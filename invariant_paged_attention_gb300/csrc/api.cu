@@ -171,6 +171,24 @@ int encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int head_d
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
+// The paged cache [slots][Hkv][head_dim] bf16 as a 3-D map whose boxes are
+// 64 columns x 1 kv head x 16 consecutive slots (128-byte swizzle); slots
+// past the end read as zeros.
+int encode_slots_map(CUtensorMap *map, const void *base, int64_t slots, int Hkv, int head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return -1;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(slots)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(Hkv) * head_dim * 2};
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return static_cast<int>(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
 // A 2-D map over `rows` rows of `cols` bf16 (row pitch cols*2 bytes) in boxes
 // of 64 columns x box_rows rows, 128-byte swizzle; rows past the end read as
 // zeros.
@@ -418,6 +436,11 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
                           tile_tokens);
     if (ce == 0) ce = encode_rows_map(&a.tm_k, k_cache, kv_rows, desc->head_dim);
     if (ce == 0) ce = encode_rows_map(&a.tm_v, v_cache, kv_rows, desc->head_dim);
+    if (ce == 0 && desc->head_dim == 256 && desc->page_size >= 16) {
+      const int64_t slots = num_pages * desc->page_size;
+      ce = encode_slots_map(&a.tm_k3, k_cache, slots, desc->num_kv_heads, desc->head_dim);
+      if (ce == 0) ce = encode_slots_map(&a.tm_v3, v_cache, slots, desc->num_kv_heads, desc->head_dim);
+    }
     if (ce != 0) return fail(BIA_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable", ce);
   }
 

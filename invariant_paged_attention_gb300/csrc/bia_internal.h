@@ -190,6 +190,9 @@ struct AttnArgs {
   // D] in 64-column boxes one row high; all SW128
   CUtensorMap tm_q, tm_k, tm_v;
   int32_t q_rows, kv_rows; // row extents of the maps (a row >= extent reads as zeros)
+  // head_dim 256 with pages of 16+ keys: the caches as 3-D maps [slots][Hkv][D]
+  // in boxes of 64 columns x 1 head x 16 slots (16 consecutive keys of one page)
+  CUtensorMap tm_k3, tm_v3;
   // multi-head latent attention on the tensor cores: q_pe rows [B*H, 64] in
   // 64 x 16-row boxes (tm_q then holds q_nope [B*H, 512] in the same boxes,
   // tm_k the ckv rows [num_pages*P, 512] in 64 x 1 boxes) and the kpe rows

@@ -165,23 +165,44 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             rows[i] = ((pg[i] << a.page_shift) + (key & page_mask)) * a.Hkv + kvh;
         }
       }
+      // With pages of 16+ keys this CTA's 16 keys of the block are 16
+      // consecutive slots of one page: when all of them are in the sequence
+      // and the page is valid, they arrive as one tiled box per 64 columns
+      // instead of 16 row gathers (the TMA issue rate of 128-byte row boxes
+      // bounds this kernel); otherwise the rows are gathered one by one.
+      const int32_t kb = key_begin + j * kKB + (kKB / kCtasW) * static_cast<int32_t>(rank);
+      const int32_t pg0 = __shfl_sync(0xffffffffu, pg[0], 0); // lane 0 holds key kb's page
+      const bool tiled = a.page_shift >= 4 && kb + kKB / kCtasW <= r.kv_len && pg0 >= 0 &&
+                         pg0 < a.num_pages;
+      const int32_t slot0 = (pg0 << a.page_shift) + (kb & page_mask);
+      const uint32_t tile_off = static_cast<uint32_t>(lane * kAtomKV + (kb - key_begin - j * kKB) * 128);
       fetch(j + 1, pg);
       bool ok = j < 2 || mbar_wait(bar(L::kKEmpty + st), ((j >> 1) - 1) & 1, a.status);
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_expect_tx(bar(L::kKFull + st), L::kKVTile);
       __syncwarp();
-      if (issues)
+      if (tiled) {
+        if (lane < kD / 64)
+          tma_load_3d_mc(sK(st) + tile_off, &a.tm_k3, 64 * lane, kvh, slot0, bar(L::kKFull + st),
+                         kMaskW);
+      } else if (issues) {
         tma_gather4_mc(sK(st) + dst_off, &a.tm_k, 64 * hh, rows[0], rows[1], rows[2], rows[3],
                        bar(L::kKFull + st), kMaskW);
+      }
       ok = j < 2 || mbar_wait(bar(L::kVEmpty + st), ((j >> 1) - 1) & 1, a.status);
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_expect_tx(bar(L::kVFull + st), L::kKVTile);
       __syncwarp();
-      if (issues)
+      if (tiled) {
+        if (lane < kD / 64)
+          tma_load_3d_mc(sV(st) + tile_off, &a.tm_v3, 64 * lane, kvh, slot0, bar(L::kVFull + st),
+                         kMaskW);
+      } else if (issues) {
         tma_gather4_mc(sV(st) + dst_off, &a.tm_v, 64 * hh, rows[0], rows[1], rows[2], rows[3],
                        bar(L::kVFull + st), kMaskW);
+      }
     }
   } else if (warp == kMmaW) {
     // ------------------------------------------------------------ MMA issuer

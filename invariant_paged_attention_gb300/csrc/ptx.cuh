@@ -195,6 +195,18 @@ __device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const void *tmap, i
                : "memory");
 }
 
+// A 3-D tiled TMA load (coordinates innermost first) written at the same
+// shared-memory offset of every CTA of the cluster in cta_mask; each
+// destination CTA's barrier at offset `bar` receives the complete_tx of the
+// bytes written into that CTA.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                               int32_t z, uint32_t bar, uint16_t cta_mask) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+               "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
+               : "memory");
+}
+
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32).
 __device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

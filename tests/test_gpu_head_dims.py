@@ -57,6 +57,8 @@ def test_d96_chunked_prefill_and_batch_invariance():
     (16, 8, 16, [(0, 300), (700, 77), (5, 1), (129, 160)], True),
     (8, 1, 1, [(0, 130), (4100, 70)], True),
     (32, 4, 16, [(10, 90), (0, 33)], False),
+    (16, 8, 16, [(4000, 300), (0, 4200), (31, 17)], True),
+    (16, 8, 32, [(1000, 250), (4090, 20)], True),
 ])
 def test_prefill_d256_matches_oracle(Hq, Hkv, P, seqs, causal):
     store = wl.PagedStore([wl.Sequence(1900 + i, p, n) for i, (p, n) in enumerate(seqs)],
@@ -105,3 +107,17 @@ def test_decode_d256_other_group_sizes(Hq, Hkv):
     call = wl.whole_prefill(store)
     out, lse = run_decode(call)
     check_rows(call, out, lse)
+
+
+@pytest.mark.parametrize("P", [16, 32, 256])
+def test_d256_prefill_bits_do_not_depend_on_the_page_size(P):
+    """With pages of 16+ keys a CTA's keys arrive as tiled boxes of whole page
+    runs (rows past the sequence still gathered); at page 1 every row is
+    gathered.  The shared-memory tiles and so the results are the same bits."""
+    seqs = [wl.Sequence(2300 + i, p, n) for i, (p, n) in enumerate([(0, 700), (4100, 90),
+                                                                    (33, 250)])]
+    ref_o, ref_l = run_prefill(wl.whole_prefill(wl.PagedStore(seqs, 16, 8, 256, 1, DEV,
+                                                              layout_seed=34)))
+    o, l = run_prefill(wl.whole_prefill(wl.PagedStore(seqs, 16, 8, 256, P, DEV,
+                                                      layout_seed=35)))
+    assert same_bits(o, ref_o) and same_bits(l, ref_l)

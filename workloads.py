@@ -353,12 +353,12 @@ def cfg4_decode(device, batch: int, lo: int = 1024, hi: int = 32768) -> PagedSto
     return PagedStore(seqs, page_size=1, device=device, layout_seed=4999 + batch, **QWEN)
 
 
-def wide_prefill(device, batch: int = 8) -> PagedStore:
+def wide_prefill(device, batch: int = 8, page_size: int = 1) -> PagedStore:
     """cfg2's lengths (uniform in [512, 8192], same seed) with head_dim 256:
-    16 q heads / 8 kv heads (a Gemma-style layout), page 1."""
+    16 q heads / 8 kv heads (a Gemma-style layout), page 1 by default."""
     lens = uniform_lengths(batch, 512, 8192, 2000)
     seqs = [Sequence(7000 + i, 0, L) for i, L in enumerate(lens)]
-    return PagedStore(seqs, 16, 8, 256, 1, device, layout_seed=7999)
+    return PagedStore(seqs, 16, 8, 256, page_size, device, layout_seed=7999)
 
 
 def wide_decode(device, B: int = 64) -> PagedStore:
