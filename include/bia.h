@@ -42,7 +42,8 @@
  * current device: the prefill kernels multicast each gathered K/V row into
  * the CTAs of a thread-block cluster, which this library does for this GPU's
  * own memory only, so a host, managed or peer-mapped pointer is refused with
- * BIA_ERR_INVALID_ARG (bia_last_error names it) before anything is enqueued.  The *_host
+ * BIA_ERR_INVALID_ARG (bia_last_error names it) before anything is enqueued.
+ * The *_host
  * arrays are read synchronously during the call (to validate and to size the
  * launch) and must equal their device copies.  All work is enqueued on
  * `stream` (a cudaStream_t; NULL = legacy default stream) on the current
@@ -56,8 +57,9 @@
  * outside [0, num_pages) is caught on the device: the row is read as zeros and
  * bit 0 of the workspace status word is set (bia_read_status).  The device
  * planner also checks the device index arrays (lengths, page counts, and the
- * bounds of a bounded call); when a check fails it computes nothing, leaves
- * out and lse unwritten and sets bit 1 of the status word.
+ * bounds of a bounded call); when a check fails it computes nothing, fills
+ * out and lse with NaN (so the failure shows in the data, also under graph
+ * replay) and sets bit 1 of the status word.
  *
  * Alignment: q, out, the caches and every bf16 row buffer start on a 16-byte
  * boundary; int32 and fp32 arrays on 4 bytes, int64 arrays on 8; a call

@@ -388,6 +388,10 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
   pa.n_units_expected = hp.n_units;
   pa.n_sunits_expected = hp.n_sunits;
   pa.part_rows_expected = hp.part_rows;
+  pa.out = static_cast<uint16_t *>(out);
+  pa.out_elems = hp.total_q * desc->num_qo_heads * desc->head_dim;
+  pa.lse = lse;
+  pa.lse_elems = hp.total_q * desc->num_qo_heads;
   pa.status = reinterpret_cast<int32_t *>(ws + w.status);
   pa.reqs = reinterpret_cast<bia::ReqInfo *>(ws + w.reqs);
   pa.group_off = reinterpret_cast<int32_t *>(ws + w.group_off);
@@ -816,6 +820,10 @@ int run_mla(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
   pa.n_groups_expected = hp.n_groups;
   pa.n_units_expected = hp.n_units;
   pa.part_rows_expected = hp.part_rows;
+  pa.out = static_cast<uint16_t *>(out);
+  pa.out_elems = hp.total_q * desc->num_heads * BIA_MLA_CKV_DIM;
+  pa.lse = lse;
+  pa.lse_elems = hp.total_q * desc->num_heads;
   pa.status = reinterpret_cast<int32_t *>(ws + w.status);
   pa.reqs = reinterpret_cast<bia::ReqInfo *>(ws + w.reqs);
   pa.group_off = reinterpret_cast<int32_t *>(ws + w.group_off);

@@ -162,6 +162,12 @@ struct PlanArgs {
   int32_t max_q_len, max_kv_len; // per-request bounds (bounded calls)
   int64_t max_total_q;            // q tokens of the call (bounded calls)
   int64_t n_groups_expected, n_units_expected, n_sunits_expected, part_rows_expected;
+  // the call's outputs: filled with NaN when the plan fails its checks, so a
+  // failure shows in the data and not only in the status word
+  uint16_t *out;
+  int64_t out_elems;
+  float *lse;      // may be NULL
+  int64_t lse_elems;
   int32_t *status;
   ReqInfo *reqs;
   int32_t *group_off, *group_cnt;

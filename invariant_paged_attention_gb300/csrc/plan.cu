@@ -205,6 +205,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       a.units[i] = Unit{-1, 0, 0, 0};
     for (int64_t i = tid; i < a.n_sunits_expected; i += kPlanThreads)
       a.sunits[i] = Unit{-1, 0, 0, 0};
+    // nothing will be computed: the outputs read NaN instead of stale values
+    for (int64_t i = tid; i < a.out_elems; i += kPlanThreads) a.out[i] = 0x7fc0u; // bf16 NaN
+    for (int64_t i = tid; a.lse && i < a.lse_elems; i += kPlanThreads) a.lse[i] = __int_as_float(0x7fc00000);
     return;
   }
 

@@ -79,11 +79,22 @@ def test_bounded_decode_matches_the_exact_call_bit_for_bit(page_size):
 
 
 def test_lengths_beyond_the_bounds_compute_nothing_and_set_the_status():
+    """Nothing is computed, the status says so, and out / lse read NaN (a
+    stale value would pass unnoticed under graph replay)."""
     store = wl.PagedStore([wl.Sequence(8800 + i, c - 1, 1) for i, c in enumerate([500, 3000])],
                           32, 8, 128, 16, DEV, layout_seed=88)
     call = wl.whole_prefill(store)
-    out, lse, status = bounded_decode(call, bia.make_bounds(1, 2999, 0))
-    assert status & STATUS_PLAN
+    st = call.store
+    desc = desc_of(st)
+    bd = bia.make_bounds(1, 2999, 0)
+    ws = torch.empty(bia.bia_decode_bounded_workspace_size(desc, bd, call.batch),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.zeros_like(call.q)  # zeros, not NaN: the call must overwrite them
+    lse = torch.zeros((call.batch, st.num_qo_heads), dtype=torch.float32, device=DEV)
+    bia.bia_decode_paged_bounded(desc, bd, call.q, st.k_cache, st.v_cache,
+                                 call.kv_indptr.to(DEV), call.kv_indices.to(DEV),
+                                 call.kv_last_page_len.to(DEV), ws, out, lse)
+    assert bia.bia_read_status(ws) & STATUS_PLAN
     assert torch.isnan(out.float()).all() and torch.isnan(lse).all()
     pstore = wl.PagedStore([wl.Sequence(8900 + i, p, n) for i, (p, n) in
                             enumerate([(0, 300), (64, 64)])], 32, 8, 128, 16, DEV, layout_seed=89)
@@ -224,3 +235,25 @@ def test_graph_replays_chunked_extend_steps_while_every_prefix_grows():
         e_o, e_l = run_prefill(calls[s])
         assert same_bits(g_o, e_o) and same_bits(g_l, e_l), s
         check_rows(calls[s], g_o, g_l, tokens_per_part=64, seed=s)
+
+
+def test_device_arrays_that_disagree_with_the_host_mirrors_give_nan():
+    """An exact call whose device index arrays differ from the host mirrors it
+    was sized from: nothing is computed, status bit 1, out and lse read NaN."""
+    store = wl.PagedStore([wl.Sequence(8850 + i, c - 1, 1) for i, c in enumerate([3000, 5000])],
+                          32, 8, 128, 1, DEV, layout_seed=885)
+    call = wl.whole_prefill(store)
+    desc = desc_of(store)
+    short = wl.make_call(wl.PagedStore([wl.Sequence(8850, 999, 1), wl.Sequence(8851, 4999, 1)],
+                                       32, 8, 128, 1, DEV, layout_seed=885),
+                         [(0, 0, 1), (1, 0, 1)])
+    ws = torch.empty(bia.bia_decode_workspace_size(desc, short.kv_indptr, short.kv_last_page_len),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.zeros_like(call.q)
+    lse = torch.zeros((2, 32), dtype=torch.float32, device=DEV)
+    # host mirrors of a 1000-key first request, device arrays of a 3000-key one
+    bia.bia_decode_paged(desc, call.q, store.k_cache, store.v_cache, call.kv_indptr.to(DEV),
+                         call.kv_indices.to(DEV), call.kv_last_page_len.to(DEV),
+                         short.kv_indptr, short.kv_last_page_len, ws, out, lse)
+    assert bia.bia_read_status(ws) & STATUS_PLAN
+    assert torch.isnan(out.float()).all() and torch.isnan(lse).all()
