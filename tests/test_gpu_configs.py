@@ -7,7 +7,8 @@ Parity coverage: the tiny prefill, the batched prefill and every decode
 batch are compared on every row of every request; the long prefix extend
 and the mixed batch's 4096-token chunk on every request, all rows of its
 first and last q tile plus a seeded sample of 128 tokens (4096 rows), and
-the off-grid chunked run also on the first and last token of every chunk.
+both chunked runs (on and off the grid) also on the first and last token of
+every chunk.
 Rows are checked a few requests at a time so the oracle's host copies stay
 small."""
 import pytest
@@ -76,11 +77,15 @@ def test_cfg3_chunked_prefill_with_prefix(capsys):
     whole = wl.whole_prefill(store)
     out, lse = run_prefill(whole)
     mx, mean, n = check_rows(whole, out, lse, tokens_per_part=128)
-    # chunks of 256 tokens start on the 32-token grid: bit-identical
+    # chunks of 256 tokens start on the 32-token grid: bit-identical, so the
+    # first and last token of every chunk are checked on the unchunked rows
     calls = wl.chunked_calls(store, 256)
     assert len(calls) == 64
     o, l = assemble(whole, calls, [run_prefill(c) for c in calls])
     assert same_bits(o, out) and same_bits(l, lse)
+    grid_edges = sorted({t for c in range(64) for t in (256 * c, 256 * c + 255)})
+    for i in range(whole.batch):
+        check_rows(whole, out, lse, part_ids=[i], tokens=grid_edges)
     # chunks of 100 tokens leave the grid: held to the oracle only, on a
     # sample and on the first and last token of every chunk
     calls = wl.chunked_calls(store, 100)
