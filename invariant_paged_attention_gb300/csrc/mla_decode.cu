@@ -46,14 +46,15 @@
 // arrival on the slot's barrier that fires when they land) into a ring of
 // 32 KB slots (two ckv pieces: one P.V accumulator's operand) plus one slot
 // for the rope piece.  A block's ckv pieces stay until its P.V is done; the
-// ring holds the first slot of the next block meanwhile.  Each thread also
-// prefetches one key's latent rows two blocks ahead into L2, so that the
-// copies issued as slots free up hit L2.
+// ring holds the first slot of the next block meanwhile.  (An L2 prefetch of
+// the rows two blocks ahead was measured slower, 3.29 against 3.85 TB/s at 16
+// heads with the L2 flushed between calls: the prefetched lines were evicted
+// before the copies reached them and DRAM read 1.36x the rows.)
 //
 // Measured (GB300, 16 heads): an M=128 N=16 MMA issues about every 90
 // cycles, close to the N=128 rate, so a block's 68 MMAs take ~6k cycles; the
 // softmax (~2.5k cycles) and the refill of the slots a P.V frees sit between
-// them, and a block takes ~10k cycles (3.1 TB/s of latent rows at 64
+// them, and a block takes ~10k cycles (3.85 TB/s of latent rows at 64
 // requests).
 //
 // Invariance: block boundaries are absolute key positions, every head's
@@ -175,9 +176,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     // block: of each pair's 256 bytes per key, and (cc < 8) of the rope row;
     // its 16 page indices are fetched a block ahead.  Each copy group ends
     // with an arrival that fires when the thread's copies have landed (full
-    // barriers count the 128 threads).  Thread pt also prefetches key pt's
-    // latent rows two blocks ahead into L2, its page index fetched a block
-    // before that.
+    // barriers count the 128 threads).
     const int cc = pt & 15, kb = pt >> 4;
     const int page_mask = (1 << a.page_shift) - 1;
     auto page_at = [&](int j, int k) -> int32_t {
@@ -189,22 +188,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 #pragma unroll
       for (int n = 0; n < 16; ++n) pg[n] = page_at(j, kb + 8 * n);
     };
-    auto prefetch_rows = [&](int j, int32_t pg) {
-      const int32_t key = key_begin + j * kKeys + pt;
-      if (pg < 0 || pg >= a.num_pages) return;
-      const int64_t row = (static_cast<int64_t>(pg) << a.page_shift) + (key & page_mask);
-      prefetch_l2(a.k_cache + row * kMlaCkvDim, kMlaCkvDim * 2);
-      prefetch_l2(a.kpe_cache + row * kMlaKpeDim, kMlaKpeDim * 2);
-    };
-    prefetch_rows(1, page_at(1, pt));
-    int32_t pf_pg = page_at(2, pt);
     const uint32_t swz = static_cast<uint32_t>(((cc & 7) ^ (kb & 7)) << 4); // key & 7 == kb & 7
     int32_t pg_next[16];
     fetch(0, pg_next);
     bool ok = true;
     for (int j = 0; j < nb && ok; ++j) {
-      prefetch_rows(j + 2, pf_pg);
-      pf_pg = page_at(j + 3, pt);
       int32_t rows[16]; // latent row of each of this thread's keys; -1: zeros
 #pragma unroll
       for (int n = 0; n < 16; ++n) {

@@ -142,12 +142,6 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global memory
-// into L2; no completion to wait for.
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // ---------------------------------------------------------------- bulk copy
 // Global -> shared bulk copy (TMA, no tensor map) of `bytes` (multiple of 16,
 // both addresses 16-byte aligned); completes `bytes` transactions on `bar`.
