@@ -242,6 +242,16 @@ int decode_on_scratch(const bia_attn_desc *desc, const void *q, const void *k_ca
                       int32_t batch, int32_t split_size, void *scratch, size_t scratch_bytes,
                       void *out, float *lse, void *stream);
 
+// Launch attribute of the kernels that follow the planner within a call:
+// programmatic stream serialization (each waits in-kernel for its
+// predecessor's completion, so its launch overlaps the predecessor's tail).
+inline cudaLaunchAttribute chained_launch_attr() {
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  return at;
+}
+
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);

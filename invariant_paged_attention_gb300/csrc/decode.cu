@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(kThreadsDec, (G <= 4 ? 2 : 1))
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
   const uint32_t sbase = smem_u32(smem);
 
+  grid_dep_wait();   // the plan (and, for streamed tiles, the prefill kernel) is complete
+  grid_dep_launch(); // the next kernel of the call may start launching
   // block = unit * Hkv + kv head: the kv heads of a unit run side by side
   const int64_t unit = blockIdx.x / a.Hkv;
   const int kvh = static_cast<int>(blockIdx.x - unit * a.Hkv);
@@ -479,8 +481,15 @@ cudaError_t launch_decode_dgm(const AttnArgs &a, cudaStream_t s) {
   }
   const int64_t blocks = a.n_units * a.Hkv;
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
-  decode_kernel<D, G, MASK><<<static_cast<unsigned>(blocks), kThreadsDec, L::kAlloc, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kThreadsDec);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {chained_launch_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, MASK>, a);
 }
 
 template <int D, int G>

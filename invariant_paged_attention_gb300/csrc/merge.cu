@@ -4,6 +4,7 @@
 // states, never on the grid.
 #include "bia_internal.h"
 #include "fold.cuh"
+#include "ptx.cuh"
 
 namespace bia {
 
@@ -70,9 +71,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_partials_kernel(const AttnArgs a) {
   const int D = a.D;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  grid_dep_wait(); // the attention kernel's partials are complete
   const int64_t token = blockIdx.x;
   if (token >= a.total_rows) return;
-  // a plan that failed its checks computed nothing: leave out unwritten
+  // a plan that failed its checks computed nothing (out already holds NaN)
   if (a.status[0] & kStatusPlanMismatch) return;
   const int b = a.qo_indptr ? owner(a.qo_indptr, a.batch, token) : static_cast<int>(token);
   const ReqInfo r = a.reqs[b];
@@ -147,14 +149,18 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t st) {
   if (a.total_rows == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>(a.total_rows);
-  if (a.D <= 128)
-    merge_partials_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(a);
-  else if (a.D <= 256) // head_dim 256: eight floats per lane
-    merge_partials_kernel<8><<<grid, kMergeWarps * 32, 0, st>>>(a);
-  else // the 512-wide latent rows of multi-head latent attention
-    merge_partials_kernel<16><<<grid, kMergeWarps * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.total_rows));
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {chained_launch_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.D <= 128) return cudaLaunchKernelEx(&cfg, merge_partials_kernel<4>, a);
+  if (a.D <= 256) // head_dim 256: eight floats per lane
+    return cudaLaunchKernelEx(&cfg, merge_partials_kernel<8>, a);
+  // the 512-wide latent rows of multi-head latent attention
+  return cudaLaunchKernelEx(&cfg, merge_partials_kernel<16>, a);
 }
 
 cudaError_t launch_merge_states(const float *v, const float *s, const int32_t *num_states,

@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   auto pair_slot = [&](int s) { return sbase + L::kRing + static_cast<uint32_t>(s) * 2 * kPiece; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kSlot);
 
+  grid_dep_wait();   // the plan is complete
+  grid_dep_launch(); // the next kernel of the call may start launching
   // block = unit * head groups + head group: a unit's head groups run side by side
   const int n_hg = (a.Hq + kHg - 1) / kHg;
   const int64_t unit = blockIdx.x / n_hg;
@@ -487,8 +489,15 @@ cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s) {
   }
   const int64_t blocks = a.n_units * ((a.Hq + kHg - 1) / kHg);
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
-  mla_decode_kernel<<<static_cast<unsigned>(blocks), kThreadsT, MlaSmem::kAlloc, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kThreadsT);
+  cfg.dynamicSmemBytes = MlaSmem::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {chained_launch_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, a);
 }
 
 } // namespace bia

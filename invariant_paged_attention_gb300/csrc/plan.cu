@@ -20,6 +20,7 @@
 // any check fails or the plan does not fit the launch, every unit is retired
 // and a status bit is set instead of reading or writing out of bounds.
 #include "bia_internal.h"
+#include "ptx.cuh"
 
 namespace bia {
 
@@ -100,6 +101,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   __shared__ int64_t s_scan[kPlanThreads / 32];
   __shared__ int s_ok;
   const int tid = threadIdx.x;
+  // the attention kernel may start launching now: it waits for this plan
+  // before reading it.  (The planner itself is launched plainly, after
+  // everything before it in the stream, since it rewrites the workspace.)
+  grid_dep_launch();
   const int32_t gt = group_tiles(a.tiles_per_unit, a.ctas);
   if (tid == 0) a.status[0] = 0;
 

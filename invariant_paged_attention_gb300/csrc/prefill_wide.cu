@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   auto sV = [&](int st) { return sbase + L::kKV + (2 * st + 1) * L::kKVTile; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kSlot);
 
+  grid_dep_wait();   // the plan is complete
+  grid_dep_launch(); // the next kernel of the call may start launching
   if (blockIdx.x >= a.n_units) return;
   const Unit u = a.units[blockIdx.x];
   if (u.b < 0) return; // plan mismatch: every unit of the launch is disabled
@@ -439,13 +441,14 @@ cudaError_t launch_wide(const AttnArgs &a, cudaStream_t s) {
   cfg.blockDim = dim3(kThreadsW);
   cfg.dynamicSmemBytes = SmemW::kAlloc;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCtasW;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = chained_launch_attr();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, prefill_wide_kernel<MASK>, a);
 }
 

@@ -100,6 +100,19 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 constexpr uint64_t kWaitLimitNs = 2000000000ull; // 2 s: far beyond any legal wait
 
+// ---------------------------------------------------------------- launch chaining
+// The kernels of one call are launched with programmatic stream serialization:
+// a kernel may start while the previous one runs, and waits here until that
+// kernel has completed and its writes are visible (a no-op without it).
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream start launching (it waits for this
+// kernel's completion before reading anything this kernel writes).
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
