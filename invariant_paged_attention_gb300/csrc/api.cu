@@ -865,8 +865,9 @@ int run_mla(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
   a.status = pa.status;
   a.q_rows = static_cast<int32_t>(q_rows);
   a.kv_rows = static_cast<int32_t>(kv_rows);
-  int ce = encode_2d_map(&a.tm_q, q_nope, q_rows, BIA_MLA_CKV_DIM, bia::kMlaHeadGroup);
-  if (ce == 0) ce = encode_2d_map(&a.tm_qpe, q_pe, q_rows, BIA_MLA_KPE_DIM, bia::kMlaHeadGroup);
+  const int hg = bia::mla_head_group(desc->num_heads);
+  int ce = encode_2d_map(&a.tm_q, q_nope, q_rows, BIA_MLA_CKV_DIM, hg);
+  if (ce == 0) ce = encode_2d_map(&a.tm_qpe, q_pe, q_rows, BIA_MLA_KPE_DIM, hg);
   if (ce == 0) ce = encode_2d_map(&a.tm_k, ckv_cache, kv_rows, BIA_MLA_CKV_DIM, 1);
   if (ce == 0) ce = encode_2d_map(&a.tm_kpe, kpe_cache, kv_rows, BIA_MLA_KPE_DIM, 1);
   if (ce != 0) return fail(BIA_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable", ce);

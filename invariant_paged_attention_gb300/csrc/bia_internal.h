@@ -258,7 +258,9 @@ cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_wide(const AttnArgs &a, cudaStream_t s); // head_dim 256
 cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s);
-constexpr int kMlaHeadGroup = 16; // q heads per CTA of the MLA decode kernel
+// q heads per CTA of the MLA kernel: 32 when the head count is a multiple of
+// 32, else 16 (the q tensor map's boxes are this many rows high)
+inline int mla_head_group(int num_heads) { return num_heads % 32 == 0 ? 32 : 16; }
 cudaError_t launch_merge_partials(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_merge_states(const float *v, const float *s, const int32_t *num_states,
                                 int64_t n, int32_t S, int32_t H, int32_t D, uint16_t *out,

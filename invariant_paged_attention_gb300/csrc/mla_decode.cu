@@ -12,24 +12,26 @@
 // 16 to 128 heads, far fewer than the 128 rows of an M=128 tile, while a
 // 128-key block fills M exactly.
 //
-// One CTA per (query token, split tile, group of 16 heads); keys in 128-key
-// blocks.  A decode call has one query token per request; an extend call
+// One CTA per (query token, split tile, group of HG heads), HG = 32 when the
+// head count is a multiple of 32, else 16; keys in 128-key blocks.  A decode call has one query token per request; an extend call
 // (bia_mla_prefill_paged) runs each of its causal query tokens the same way,
 // against the keys up to its own position, so a token's bits depend only on
 // its request's keys and the split size: not on the batch, and not on how
 // the extend is chunked.  Per block:
-//   S^T = C Q^T     M=128 keys, N=16 heads, K=512+64: A = the latent rows
-//                   (K-major, 64-column SW128 pieces), B = the 16 heads'
+//   S^T = C Q^T     M=128 keys, N=HG heads, K=512+64: A = the latent rows
+//                   (K-major, 64-column SW128 pieces), B = the group's
 //                   q_nope / q_pe (K-major), fp32 accumulator in TMEM
 //   softmax         thread t of a warpgroup = key t of the block (TMEM lane
-//                   t) reads its group's 8 heads' scores; per-head block max =
+//                   t) reads its warpgroup's HG/2 heads' scores; per-head block max =
 //                   redux over the warp, then over the group's 4 warps through
 //                   shared memory (the same value on every thread of the
 //                   group); lazy online softmax (the running
 //                   max moves only when the block max exceeds it by more than
 //                   2^8; O is then rescaled in TMEM); P = 2^(s - m) as bf16
-//                   into shared memory, row t = key t (MN-major operand)
-//   O^T += C^T P^T  four accumulators of M=128 latent columns, N=16 heads,
+//                   into shared memory, row t = key t (MN-major operand;
+//                   128-byte swizzle for 16 heads, 64-byte rows in the
+//                   64-byte swizzle for 32)
+//   O^T += C^T P^T  four accumulators of M=128 latent columns, N=HG heads,
 //                   K=128 keys: A = the same latent pieces read MN-major
 //                   (two 64-column pieces side by side), B = P
 // Each thread keeps its own keys' partial row sums per head; the epilogue
@@ -37,10 +39,11 @@
 // o = O^T / l and lse (bf16 rows for a request with one split, else fp32
 // partials).
 //
-// Warp roles (13 warps): 0-7 softmax + epilogue (two warpgroups of 8 heads
-// each, a thread per key), 8 owns TMEM and issues every MMA from one thread,
-// 9-12 copy: one thread loads the 16 heads' q (2-D TMA
-// boxes), and the 128 threads copy the paged latent rows with 16-byte cp.async
+// Warp roles: 0-7 softmax + epilogue (two warpgroups of HG/2 heads each, a
+// thread per key), 8 owns TMEM and issues every MMA from one thread, then the
+// copy warps (four for 16 heads, two for 32, which leaves the softmax threads
+// the registers for their 16 heads): one thread loads the group's q (2-D TMA
+// boxes), and the copy threads move the paged latent rows with 16-byte cp.async
 // straight into the swizzled operand layout (keys past the split or on a bad
 // page are zero-filled; each thread's copies of a ring slot end with an
 // arrival on the slot's barrier that fires when they land) into a ring of
@@ -54,8 +57,10 @@
 // Measured (GB300, 16 heads): an M=128 N=16 MMA issues about every 90
 // cycles, close to the N=128 rate, so a block's 68 MMAs take ~6k cycles; the
 // softmax (~2.5k cycles) and the refill of the slots a P.V frees sit between
-// them, and a block takes ~10k cycles (3.85 TB/s of latent rows at 64
-// requests).
+// them, and a block takes ~10k cycles (3.88 TB/s of latent rows at 64
+// requests).  The MMA count per block does not depend on N, so a group of 32
+// heads does the work of two groups of 16 in about the time of one: 64 heads
+// 1.15 -> 1.76 TB/s and 128 heads 0.59 -> 0.92 TB/s, the same bits.
 //
 // Invariance: block boundaries are absolute key positions, every head's
 // column of the MMAs is computed on its own, and the lazy-rescale decisions
@@ -68,35 +73,69 @@ namespace bia {
 
 namespace {
 
-constexpr int kHg = kMlaHeadGroup;           // 16 heads: the MMA's N
 constexpr int kKeys = 128;                   // keys per block: the MMA's M
 constexpr int kPiece = kKeys * 128;          // 128 rows x 64 bf16, SW128
 constexpr int kCkvPieces = kMlaCkvDim / 64;  // 8
 constexpr int kPairs = 5;                    // ring slots of two ckv pieces
-constexpr int kHs = 8;             // heads per softmax warpgroup (two warpgroups)
-constexpr int kThreadsT = 416;
 constexpr int kMmaWarpT = 8;
-constexpr int kProdWarpT = 9;      // warps 9-12 copy the latent rows
+constexpr int kProdWarpT = 9;      // warps 9.. copy the latent rows
 constexpr float kLazyT = 8.0f; // log2 units
 
+// A CTA takes HG heads (the MMAs' N): 16, or 32 when the head count is a
+// multiple of 32 (half the CTAs over the same rows and half the MMAs per
+// head).  Two softmax warpgroups take HG/2 heads each.  For 32 heads P is
+// kept with 64-byte rows in the 64-byte swizzle, and two copy warps instead of
+// four leave the softmax threads the registers of their 16 heads.
+template <int HG>
+struct MlaCfg {
+  static constexpr int kHs = HG / 2;                   // heads per softmax warpgroup
+  static constexpr int kProdWarps = HG == 16 ? 4 : 2;  // copy warps
+  static constexpr int kThreads = (kProdWarpT + kProdWarps) * 32;
+  static constexpr int kPRow = HG == 16 ? 128 : 64;    // bytes per key row of P
+  static constexpr int kTmemCols = HG == 16 ? 128 : 256;
+};
+
+template <int HG>
 struct MlaSmem {
-  static constexpr int kQPiece = kHg * 128;           // 16 heads x 64 columns
+  static constexpr int kQPiece = HG * 128;             // HG heads x 64 columns
   static constexpr int kQ = 0;                         // 9 q pieces (8 ckv + rope)
-  static constexpr int kP = kQ + 9 * kQPiece;          // P: 128 keys x 128-byte rows
-  static constexpr int kRing = kP + kPiece;            // kPairs slots of 2 pieces
+  static constexpr int kP = kQ + 9 * kQPiece;          // P: 128 keys x kPRow-byte rows
+  static constexpr int kRing = kP + kKeys * MlaCfg<HG>::kPRow; // kPairs slots of 2 pieces
   static constexpr int kKpe = kRing + kPairs * 2 * kPiece;
   static constexpr int kBar = kKpe + kPiece;
   static constexpr int bQFull = 0, bPairFull = 1, bPairEmpty = 1 + kPairs,
                        bKpeFull = 1 + 2 * kPairs, bKpeEmpty = bKpeFull + 1, bSFull = bKpeEmpty + 1,
                        bPFull = bSFull + 1, bPVDone = bPFull + 1, kNumBars = bPVDone + 1;
-  static constexpr int kRed = kBar + 256;              // float [2][2 groups][4 warps][8 heads]
-  static constexpr int kLred = kRed + 2 * 4 * kHg * 4; // float [2 groups][4 warps][8 heads]
-  static constexpr int kSlot = kLred + 4 * kHg * 4;
+  static constexpr int kRed = kBar + 256;              // float [2][2 groups][4 warps][HG/2 heads]
+  static constexpr int kLred = kRed + 2 * 4 * HG * 4;  // float [2 groups][4 warps][HG/2 heads]
+  static constexpr int kSlot = kLred + 4 * HG * 4;
   static constexpr int kBytes = kSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kRing % 1024 == 0, "ring slots on the 128-byte swizzle period");
   static_assert(kNumBars * 8 <= 256, "barrier area");
   static_assert(kAlloc <= 232448, "shared memory per CTA");
 };
+
+// Byte offset of 16-byte chunk c of key row t of P: the 128-byte swizzle of
+// 128-byte rows (16 heads), or the 64-byte swizzle of 64-byte rows (32 heads:
+// chunk bits 4-5 XOR address bits 7-8).
+template <int HG>
+__device__ __forceinline__ uint32_t p_chunk(uint32_t t, uint32_t c) {
+  if constexpr (HG == 16) return sw128(t, c);
+  else return t * 64u + ((c ^ ((t >> 1) & 3u)) << 4);
+}
+
+// TMEM load of n = HG/2 consecutive 32-bit columns (a warp's 32 lanes).
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 8) tmem_ld8(taddr, r);
+  else tmem_ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 8) tmem_st8(taddr, r);
+  else tmem_st16(taddr, r);
+}
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -104,12 +143,17 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-__global__ void __launch_bounds__(kThreadsT, 1)
+template <int HG>
+__global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ AttnArgs a) {
-  using L = MlaSmem;
+  using L = MlaSmem<HG>;
+  constexpr int kHg = HG;
+  constexpr int kHs = MlaCfg<HG>::kHs;
+  constexpr int kProdThreads = MlaCfg<HG>::kProdWarps * 32;
+  constexpr int kKeyStep = kProdThreads / 16; // keys between a copy thread's keys
   constexpr uint32_t kIdescS = idesc_bf16_ab(128, kHg, false, false);
   constexpr uint32_t kIdescPV = idesc_bf16_ab(128, kHg, true, true);
-  constexpr uint32_t kTmemCols = 128;
+  constexpr uint32_t kTmemCols = MlaCfg<HG>::kTmemCols;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -144,10 +188,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   if (tid == 0) {
     mbar_init(bar(L::bQFull), 1);
     for (int s = 0; s < kPairs; ++s) {
-      mbar_init(bar(L::bPairFull + s), 128); // one arrival per producer thread
+      mbar_init(bar(L::bPairFull + s), kProdThreads); // one arrival per copy thread
       mbar_init(bar(L::bPairEmpty + s), 1);
     }
-    mbar_init(bar(L::bKpeFull), 128);
+    mbar_init(bar(L::bKpeFull), kProdThreads);
     mbar_init(bar(L::bKpeEmpty), 1);
     mbar_init(bar(L::bSFull), 1);
     mbar_init(bar(L::bPFull), 8); // one arrival per softmax warp
@@ -158,14 +202,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S^T [0,16) (lanes = keys), O^T of latent columns
-  // 128*mb .. 128*mb+127 at [32+16mb, 48+16mb) (lanes = latent columns)
+  // TMEM columns: S^T [0,HG) (lanes = keys), O^T of latent columns
+  // 128*mb .. 128*mb+127 at [2HG+HG*mb, 3HG+HG*mb) (lanes = latent columns)
   const uint32_t tS = tmem;
-  auto tO = [&](int mb) { return tmem + 32u + 16u * static_cast<uint32_t>(mb); };
+  auto tO = [&](int mb) {
+    return tmem + 2u * kHg + static_cast<uint32_t>(kHg) * static_cast<uint32_t>(mb);
+  };
 
   if (warp >= kProdWarpT) {
     // ------------------------------------------------------------ producers
-    const int pt = tid - kProdWarpT * 32; // 0..127
+    const int pt = tid - kProdWarpT * 32; // 0..kProdThreads-1
     // rows past total_q * H read as zeros
     const int32_t q_row = static_cast<int32_t>(q_token * a.Hq + hg * kHg);
     if (pt == 0 && nb > 0) {
@@ -174,11 +220,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         tma_load_2d(sbase + L::kQ + p * L::kQPiece, &a.tm_q, 64 * p, q_row, bar(L::bQFull));
       tma_load_2d(sbase + L::kQ + kCkvPieces * L::kQPiece, &a.tm_qpe, 0, q_row, bar(L::bQFull));
     }
-    // Thread pt copies 16-byte chunk cc of keys kb, kb+8, ..., kb+120 of every
-    // block: of each pair's 256 bytes per key, and (cc < 8) of the rope row;
-    // its 16 page indices are fetched a block ahead.  Each copy group ends
-    // with an arrival that fires when the thread's copies have landed (full
-    // barriers count the 128 threads).
+    // Thread pt copies 16-byte chunk cc of keys kb, kb+kKeyStep, ... of every
+    // block (128/kKeyStep keys): of each pair's 256 bytes per key, and
+    // (cc < 8) of the rope row; its page indices are fetched a block ahead.
+    // Each copy group ends with an arrival that fires when the thread's copies
+    // have landed (full barriers count the copy threads).
     const int cc = pt & 15, kb = pt >> 4;
     const int page_mask = (1 << a.page_shift) - 1;
     auto page_at = [&](int j, int k) -> int32_t {
@@ -186,19 +232,23 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       return (j < nb && key < key_end)
                  ? __ldg(a.kv_indices + r.page_base + (key >> a.page_shift)) : -1;
     };
-    auto fetch = [&](int j, int32_t (&pg)[16]) {
+    constexpr int kNk = kKeys / kKeyStep; // keys per copy thread per block
+    auto fetch = [&](int j, int32_t (&pg)[kNk]) {
 #pragma unroll
-      for (int n = 0; n < 16; ++n) pg[n] = page_at(j, kb + 8 * n);
+      for (int n = 0; n < kNk; ++n) pg[n] = page_at(j, kb + kKeyStep * n);
     };
-    const uint32_t swz = static_cast<uint32_t>(((cc & 7) ^ (kb & 7)) << 4); // key & 7 == kb & 7
-    int32_t pg_next[16];
+    // swizzle of chunk cc in key row k of a 128-byte-swizzled piece
+    auto swz = [&](int n) {
+      return static_cast<uint32_t>(((cc & 7) ^ ((kb + kKeyStep * n) & 7)) << 4);
+    };
+    int32_t pg_next[kNk];
     fetch(0, pg_next);
     bool ok = true;
     for (int j = 0; j < nb && ok; ++j) {
-      int32_t rows[16]; // latent row of each of this thread's keys; -1: zeros
+      int32_t rows[kNk]; // latent row of each of this thread's keys; -1: zeros
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int32_t key = key_begin + j * kKeys + kb + 8 * n;
+      for (int n = 0; n < kNk; ++n) {
+        const int32_t key = key_begin + j * kKeys + kb + kKeyStep * n;
         rows[n] = -1;
         if (key < key_end) {
           if (pg_next[n] < 0 || pg_next[n] >= a.num_pages)
@@ -217,11 +267,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             if (!ok) break;
           }
           if (cc < 8) {
-            const uint32_t dbase = sbase + L::kKpe + swz;
+            const uint32_t dbase = sbase + L::kKpe;
             const uint16_t *src0 = a.kpe_cache + cc * 8;
 #pragma unroll
-            for (int n = 0; n < 16; ++n)
-              cp_async16(dbase + (kb + 8 * n) * 128,
+            for (int n = 0; n < kNk; ++n)
+              cp_async16(dbase + (kb + kKeyStep * n) * 128 + swz(n),
                          src0 + static_cast<int64_t>(max(rows[n], 0)) * kMlaKpeDim, rows[n] >= 0);
           }
           cp_async_arrive(bar(L::bKpeFull));
@@ -233,11 +283,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           ok = mbar_wait(bar(L::bPairEmpty + s), ((c / kPairs) - 1) & 1, a.status);
           if (!ok) break;
         }
-        const uint32_t dbase = pair_slot(s) + (cc >> 3) * kPiece + swz;
+        const uint32_t dbase = pair_slot(s) + (cc >> 3) * kPiece;
         const uint16_t *src0 = a.k_cache + 128 * q + cc * 8;
 #pragma unroll
-        for (int n = 0; n < 16; ++n)
-          cp_async16(dbase + (kb + 8 * n) * 128,
+        for (int n = 0; n < kNk; ++n)
+          cp_async16(dbase + (kb + kKeyStep * n) * 128 + swz(n),
                      src0 + static_cast<int64_t>(max(rows[n], 0)) * kMlaCkvDim, rows[n] >= 0);
         cp_async_arrive(bar(L::bPairFull + s));
       }
@@ -286,10 +336,14 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
           const int c = 4 * j + mb, s = c % kPairs;
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_bf16_ss(tO(mb), desc_sw128(pair_slot(s) + kk * 2048, kPiece, 1024),
-                        desc_sw128(sbase + L::kP + kk * 2048, kPiece, 1024), kIdescPV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            // P: 16 keys a step; 8-key groups 8*kPRow bytes apart
+            const uint64_t dp =
+                HG == 16 ? desc_sw128(sbase + L::kP + kk * 2048, kPiece, 1024)
+                         : desc_sw64(sbase + L::kP + kk * 1024, 8192, 512);
+            mma_bf16_ss(tO(mb), desc_sw128(pair_slot(s) + kk * 2048, kPiece, 1024), dp,
+                        kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit(bar(L::bPairEmpty + s));
         }
         mma_commit(bar(L::bPVDone));
@@ -320,7 +374,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       }
       tc_fence_after();
       uint32_t v[kHs];
-      tmem_ld8(tS + h0 + lane_base, v);
+      tmem_ld_n<kHs>(tS + h0 + lane_base, v);
       tmem_wait_ld();
       const bool valid = key_begin + j * kKeys + t < key_end;
       float s[kHs];
@@ -390,18 +444,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 #pragma unroll
         for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
           uint32_t o[kHs];
-          tmem_ld8(tO(mb) + h0 + lane_base, o);
+          tmem_ld_n<kHs>(tO(mb) + h0 + lane_base, o);
           tmem_wait_ld();
 #pragma unroll
           for (int h = 0; h < kHs; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-          tmem_st8(tO(mb) + h0 + lane_base, o);
+          tmem_st_n<kHs>(tO(mb) + h0 + lane_base, o);
         }
         tmem_wait_st();
       }
-      // P row of key t: this group's 8 heads are 16-byte chunk gs of the row
-      sts128(sbase + L::kP + sw128(t, gs),
-             make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                        pack_bf16(p[6], p[7])));
+      // P row of key t: this group's heads are 16-byte chunks gs*kHs/8 .. of
+      // the row (8 heads a chunk)
+#pragma unroll
+      for (int c = 0; c < kHs / 8; ++c)
+        sts128(sbase + L::kP + p_chunk<HG>(t, gs * (kHs / 8) + c),
+               make_uint4(pack_bf16(p[8 * c + 0], p[8 * c + 1]), pack_bf16(p[8 * c + 2], p[8 * c + 3]),
+                          pack_bf16(p[8 * c + 4], p[8 * c + 5]), pack_bf16(p[8 * c + 6], p[8 * c + 7])));
       fence_proxy_async(); // P is read by the MMA (async proxy)
       tc_fence_before();
       __syncwarp();
@@ -444,7 +501,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
       uint32_t o[kHs];
       if (have) {
-        tmem_ld8(tO(mb) + h0 + lane_base, o);
+        tmem_ld_n<kHs>(tO(mb) + h0 + lane_base, o);
         tmem_wait_ld();
       }
       const int d = mb * 128 + t; // latent column of this thread
@@ -475,29 +532,34 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
 }
 
-} // namespace
-
-cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s) {
-  if (a.n_units == 0) return cudaSuccess;
+template <int HG>
+cudaError_t launch_mla_hg(const AttnArgs &a, cudaStream_t s) {
+  using L = MlaSmem<HG>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MlaSmem::kAlloc);
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<HG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int64_t blocks = a.n_units * ((a.Hq + kHg - 1) / kHg);
+  const int64_t blocks = a.n_units * ((a.Hq + HG - 1) / HG);
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(kThreadsT);
-  cfg.dynamicSmemBytes = MlaSmem::kAlloc;
+  cfg.blockDim = dim3(MlaCfg<HG>::kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[1] = {chained_launch_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, a);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<HG>, a);
+}
+
+} // namespace
+
+cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s) {
+  if (a.n_units == 0) return cudaSuccess;
+  return mla_head_group(a.Hq) == 32 ? launch_mla_hg<32>(a, s) : launch_mla_hg<16>(a, s);
 }
 
 } // namespace bia

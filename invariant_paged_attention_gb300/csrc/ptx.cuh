@@ -368,6 +368,19 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// The same with the 64-byte swizzle (layout type 4): rows of 64 bytes, the
+// 16-byte chunk index XOR-ed with address bits 7-8.
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
 // 4-5 = 1), bf16 A and B (bits 7-9, 10-12 = 1), A K-major (bit 15 = 0),
 // B K-major or MN-major (bit 16), N/8 at bits 17-22, M/16 at bits 24-28.
