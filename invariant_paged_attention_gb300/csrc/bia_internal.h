@@ -37,7 +37,7 @@ struct ReqInfo {
   int32_t nsp;      // split-KV tiles of the request's last q tile (max over tiles)
   int64_t rowbase;  // first partial row (rows of [Hq, D] fp32), -1 if none
   int32_t page_base;// kv_indptr[b]
-  int32_t pad;
+  int32_t mbase;    // rows to merge (tokens of multi-split q tiles) of earlier requests
 };
 static_assert(sizeof(ReqInfo) == 32, "ReqInfo layout");
 
@@ -79,6 +79,25 @@ __host__ __device__ inline int32_t tile_splits(int32_t q_len, int32_t kv_len, in
   int32_t last = tile_last_key(q_len, kv_len, tile, tile_tokens, causal);
   return last < 0 ? 1 : last / split + 1;
 }
+
+// First in-call token of a request whose q tile spans more than one split
+// (q_len if none).  A tile's last key grows with the tile index (causal) or
+// is the same for every tile, so such tiles are a suffix of the request: the
+// rows the merge folds are tokens merge_first_token .. q_len-1.
+__host__ __device__ inline int32_t merge_first_token(int32_t q_len, int32_t kv_len,
+                                                     int32_t tile_tokens, int32_t causal,
+                                                     int32_t split) {
+  if (q_len <= 0 || kv_len - 1 < split) return q_len; // every key in split 0
+  if (!causal) return 0;
+  const int32_t need = split + 1 - (kv_len - q_len); // in-call tokens the tile must reach
+  if (need > q_len) return q_len;
+  const int32_t tile = need <= tile_tokens ? 0 : (need + tile_tokens - 1) / tile_tokens - 1;
+  return tile * tile_tokens;
+}
+
+// Slot of the workspace status array holding the number of rows to merge
+// (written by the planner; slot 0 is the status word).
+constexpr int kStatusMergeRows = 1;
 
 // A prefill request whose last q tile holds a single token (a one-token
 // extend, or the one-token tail of a longer chunk) has that tile streamed by

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   // ---- A: per request
   const int per = (a.batch + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(a.batch, tid * per), hi = min(a.batch, lo + per);
-  int64_t my_groups = 0, my_rows = 0, my_sunits = 0;
+  int64_t my_groups = 0, my_rows = 0, my_sunits = 0, my_merge = 0;
   bool bad = false;
   if (tid == 0) {
     bad = a.kv_indptr[0] < 0 || (a.qo_indptr && a.qo_indptr[0] != 0);
@@ -124,7 +124,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int32_t nsp = tiles > 0 ? tile_splits(q_len, kv_len, tiles - 1, a.tile_tokens,
                                                 a.causal, a.split) : 1;
     my_groups += (tensor_tiles(q_len, a.tile_tokens, a.stream) + gt - 1) / gt;
-    if (nsp > 1) my_rows += static_cast<int64_t>(q_len) * nsp;
+    if (nsp > 1) {
+      my_rows += static_cast<int64_t>(q_len) * nsp;
+      my_merge += q_len - merge_first_token(q_len, kv_len, a.tile_tokens, a.causal, a.split);
+    }
     if (streamed_tail(q_len, a.tile_tokens, a.stream)) my_sunits += nsp;
   }
   const bool any_bad = __syncthreads_or(bad) != 0;
@@ -132,6 +135,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   int64_t group = block_exclusive_scan<int64_t>(my_groups, s_scan, &total_groups);
   int64_t row = block_exclusive_scan<int64_t>(my_rows, s_scan, &total_rows);
   int64_t sunit = block_exclusive_scan<int64_t>(my_sunits, s_scan, &total_sunits);
+  int64_t total_merge;
+  int64_t mrow = block_exclusive_scan<int64_t>(my_merge, s_scan, &total_merge);
   // every thread sees the same totals: the streamed units below are written
   // only when they fit the host-sized list
   const bool sizes_ok =
@@ -144,6 +149,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   if (tid == 0) {
     s_ok = sizes_ok;
     if (s_ok) a.group_off[a.batch] = static_cast<int32_t>(total_groups);
+    a.status[kStatusMergeRows] = sizes_ok ? static_cast<int32_t>(total_merge) : 0;
   }
   for (int b = lo; b < hi; ++b) {
     int32_t q_start, q_len, kv_len;
@@ -165,8 +171,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     r.nsp = nsp;
     r.rowbase = rows > 0 ? row : -1;
     r.page_base = a.kv_indptr[b];
-    r.pad = 0;
+    r.mbase = static_cast<int32_t>(mrow);
     a.reqs[b] = r;
+    if (nsp > 1) mrow += q_len - merge_first_token(q_len, kv_len, a.tile_tokens, a.causal, a.split);
     a.group_off[b] = static_cast<int32_t>(group);
     group += (tensor_tiles(q_len, a.tile_tokens, a.stream) + gt - 1) / gt;
     row += rows;
