@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbia.so")
-SOURCES = ["api.cu", "plan.cu", "merge.cu", "decode.cu", "prefill.cu", "static_ws.cu", "append.cu", "prefill_wide.cu", "mla_decode.cu"]
+SOURCES = ["api.cu", "plan.cu", "merge.cu", "decode.cu", "decode_tc.cu", "prefill.cu", "static_ws.cu", "append.cu", "prefill_wide.cu", "mla_decode.cu"]
 HEADERS = ["bia_internal.h", "ptx.cuh", "fold.cuh", "softmax_rows.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

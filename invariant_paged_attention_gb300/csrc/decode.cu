@@ -512,6 +512,7 @@ cudaError_t launch_decode_d(const AttnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
+  if (decode_tc_supported(a)) return launch_decode_tc(a, s);
   // head_dim 96 runs on the 128-wide layout, zero-padded
   if (a.D == 256) return launch_decode_d<256>(a, s);
   return a.D > 64 ? launch_decode_d<128>(a, s) : launch_decode_d<64>(a, s);

@@ -218,6 +218,19 @@ __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *tmap, i
 __device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// The same barrier, returning whether `pred` held on any of the `count`
+// threads: a decision every participant takes the same way.
+__device__ __forceinline__ bool bar_any_named(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\t"
+               "setp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.or.pred q, %2, %3, p;\n\t"
+               "selp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+               : "memory");
+  return r != 0;
+}
 
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
