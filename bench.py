@@ -742,13 +742,13 @@ def main():
     peaks, peak_kind = load_peaks()
     # counters are keyed by the kernel's own translation unit
     pre_src = ["invariant_paged_attention_gb300/csrc/prefill.cu"]
-    dec_src = ["invariant_paged_attention_gb300/csrc/decode.cu"]
+    dec_src = ["invariant_paged_attention_gb300/csrc/decode_tc.cu"]
     roofline = roofline_of("tensor", flops, pk_avg * 1e3, peaks, peak_kind, "prefill_kernel<128>",
                            traffic_from_profiles("prefill_kernel<128>", pre_src, flops)) \
         if prefill else None
     dec_roof = roofline_of("hbm", dbytes, dk_avg * 1e3, peaks, peak_kind,
-                           "decode_kernel<128,4,false>",
-                           traffic_from_profiles("decode_kernel<128,4,false>", dec_src, dbytes)) \
+                           "decode_tc_kernel<4,false>",
+                           traffic_from_profiles("decode_tc_kernel<4,false>", dec_src, dbytes)) \
         if decode else None
 
     # ---- end to end through host buffers: each step copies its inputs from
@@ -888,7 +888,7 @@ def main():
         f = decode_call(dst, dc)
         cm, km, nl = leg.run([f], cs, cw)
         put("cfg5_decodes", "hbm", kv_bytes(dc, 8, 128), cm, km, nl,
-            "decode_kernel<128,4,false>", "32 decodes at 131072 context, page 16")
+            "decode_tc_kernel<4,false>", "32 decodes at 131072 context, page 16")
         del pst, dst, pc, dc, f
         for B in (1, 8, 64):
             st = wl.cfg4_decode(dev, B)
@@ -896,7 +896,7 @@ def main():
             f = decode_call(st, c)
             cm, km, nl = leg.run([f], cs, cw)
             put(f"cfg4_b{B}", "hbm", kv_bytes(c, 8, 128), cm, km, nl,
-                "decode_kernel<128,4,false>", f"{B} decodes, ctx U[1024,32768], page 1")
+                "decode_tc_kernel<4,false>", f"{B} decodes, ctx U[1024,32768], page 1")
             del st, c, f
         del flush
         torch.cuda.empty_cache()

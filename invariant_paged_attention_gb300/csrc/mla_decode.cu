@@ -41,8 +41,8 @@
 //
 // Warp roles: 0-7 softmax + epilogue (two warpgroups of HG/2 heads each, a
 // thread per key), 8 owns TMEM and issues every MMA from one thread, then the
-// copy warps (four for 16 heads, two for 32, which leaves the softmax threads
-// the registers for their 16 heads): one thread loads the group's q (2-D TMA
+// copy warps (eight for 16 heads, four for 32, within the registers the
+// softmax threads of 32 heads need): one thread loads the group's q (2-D TMA
 // boxes), and the copy threads move the paged latent rows with 16-byte cp.async
 // straight into the swizzled operand layout (keys past the split or on a bad
 // page are zero-filled; each thread's copies of a ring slot end with an
@@ -89,7 +89,7 @@ constexpr float kLazyT = 8.0f; // log2 units
 template <int HG>
 struct MlaCfg {
   static constexpr int kHs = HG / 2;                   // heads per softmax warpgroup
-  static constexpr int kProdWarps = HG == 16 ? 4 : 2;  // copy warps
+  static constexpr int kProdWarps = HG == 16 ? 8 : 4;  // copy warps
   static constexpr int kThreads = (kProdWarpT + kProdWarps) * 32;
   static constexpr int kPRow = HG == 16 ? 128 : 64;    // bytes per key row of P
   static constexpr int kTmemCols = HG == 16 ? 128 : 256;
