@@ -274,7 +274,7 @@ inline cudaLaunchAttribute chained_launch_attr() {
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const AttnArgs &a, cudaStream_t s);
-// The tensor-core decode (head_dim 128, G in {1, 2, 4, 8, 16}); launch_decode
+// The tensor-core decode (head_dim 128, G in {1, 2, 4, 8}); launch_decode
 // takes it whenever it applies.
 bool decode_tc_supported(const AttnArgs &a);
 cudaError_t launch_decode_tc(const AttnArgs &a, cudaStream_t s);

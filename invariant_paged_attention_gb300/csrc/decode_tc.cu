@@ -2,7 +2,7 @@
 // TMEM): the same units as decode.cu (request, split-KV tile, kv head; fixed
 // split tiles anchored at key 0, "sglang PR #10417 [POC] Support
 // deterministic inference", Modifications), with the keys as the MMAs' M and
-// the G query heads of the kv head as N (padded to 16):
+// the G (1, 2, 4 or 8) query heads of the kv head as N (padded to 16):
 //   S^T = K Q^T      M=128 keys of a block, N=16, K=128: A = the key rows
 //                    (two 64-column SW128 pieces), B = the G heads' q rows
 //   softmax          thread t = key t of the block (TMEM lane t) reads its
@@ -58,7 +58,7 @@ constexpr int kProdWarpTc = 5; // the first copy warp
 
 // Copy warps for G heads: as many as the registers of the CTA allow (the copy
 // rate grows with the number of threads issuing cp.async).
-__host__ __device__ constexpr int tc_copy_warps(int G) { return G <= 4 ? 16 : G == 8 ? 8 : 4; }
+__host__ __device__ constexpr int tc_copy_warps(int G) { return G <= 4 ? 16 : 8; }
 constexpr float kLazyTc = 8.0f; // log2 units
 
 struct DecTcSmem {
@@ -591,7 +591,7 @@ cudaError_t launch_tc_g(const AttnArgs &a, cudaStream_t s) {
 } // namespace
 
 bool decode_tc_supported(const AttnArgs &a) {
-  return a.D == kDT && (a.G == 1 || a.G == 2 || a.G == 4 || a.G == 8 || a.G == 16);
+  return a.D == kDT && (a.G == 1 || a.G == 2 || a.G == 4 || a.G == 8);
 }
 
 cudaError_t launch_decode_tc(const AttnArgs &a, cudaStream_t s) {
@@ -601,7 +601,6 @@ cudaError_t launch_decode_tc(const AttnArgs &a, cudaStream_t s) {
   case 2: return launch_tc_g<2>(a, s);
   case 4: return launch_tc_g<4>(a, s);
   case 8: return launch_tc_g<8>(a, s);
-  case 16: return launch_tc_g<16>(a, s);
   default: return cudaErrorInvalidValue;
   }
 }

@@ -59,6 +59,7 @@ DECODE_CASES = [
     (8, 8, 64, 16, [300, 2048 * 3 + 5]),
     (16, 8, 128, 4, [999, 4100]),
     (64, 8, 128, 1, [2500, 10]),
+    (8, 8, 128, 1, [3000, 5, 2049]),
     (4, 1, 64, 1, [3000, 64]),
     # the larger pages the header allows
     (32, 8, 128, 32, [5000, 33, 1]),
