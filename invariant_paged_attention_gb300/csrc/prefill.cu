@@ -244,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         mma_commit(bar(L::kSFull + t));
       };
-      auto issue_pv = [&](int t, int j, int nb) {
+      auto issue_pv = [&](int t, int j, int nb, bool ready) {
         const int st = j & 1;
-        ok = ok && mbar_wait(bar(L::kPFull + t), j & 1, a.status);
+        ok = ok && (ready || mbar_wait(bar(L::kPFull + t), j & 1, a.status));
         if (!ok) return;
         tc_fence_after();
         const uint64_t dv = st ? dV1 : dV0;
@@ -267,12 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       if (ok && 2 < n_blocks) mma_commit_mc(bar(L::kKEmpty + 0), kClusterMask);
       for (int j = 0; j < n_blocks && ok; ++j) {
         const int st = j & 1;
-        ok = mbar_wait(bar(L::kVFull + st), (j >> 1) & 1, a.status);
+        // a barrier's answer takes ~170 cycles to come back even when its
+        // phase is complete: ask the block's four barriers at once and use
+        // the answers in order (a blocking bounded wait only where one is
+        // not complete yet)
+        const bool v_rdy = mbar_try(bar(L::kVFull + st), (j >> 1) & 1);
+        const bool pa_rdy = j < nb0 && mbar_try(bar(L::kPFull + 0), j & 1);
+        const bool k_rdy = j + 1 < n_blocks &&
+                           mbar_try(bar(L::kKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
+        const bool pb_rdy = j < nb1 && mbar_try(bar(L::kPFull + 1), j & 1);
+        ok = v_rdy || mbar_wait(bar(L::kVFull + st), (j >> 1) & 1, a.status);
         if (!ok) break;
-        if (j < nb0) issue_pv(0, j, nb0);
-        if (j + 1 < n_blocks) wait_k(j + 1);
+        if (j < nb0) issue_pv(0, j, nb0, pa_rdy);
+        if (j + 1 < n_blocks) {
+          ok = ok && (k_rdy || mbar_wait(bar(L::kKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1,
+                                         a.status));
+          if (ok) tc_fence_after();
+        }
         if (j + 1 < nb0) issue_s(0, j + 1);
-        if (j < nb1) issue_pv(1, j, nb1);
+        if (j < nb1) issue_pv(1, j, nb1, pb_rdy);
         if (j + 1 < nb1) issue_s(1, j + 1);
         if (!ok) break;
         if (j + 2 < n_blocks) mma_commit_mc(bar(L::kVEmpty + st), kClusterMask);
