@@ -366,10 +366,16 @@ __global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
       m[h] = -INFINITY;
       l[h] = 0.f;
     }
+    // A wait that runs out ends this thread's loop; it then still arrives at
+    // the named barriers of the blocks it did not reach (drain below), so
+    // every thread of the group makes the same nb + 1 arrivals and no
+    // barrier waits for a thread that has left.
     bool failed = false;
+    int drain_from = nb; // first block whose named barrier this thread has not passed
     for (int j = 0; j < nb; ++j) {
       if (!mbar_wait(bar(L::bSFull), j & 1, a.status)) {
         failed = true;
+        drain_from = j;
         break;
       }
       tc_fence_after();
@@ -437,6 +443,7 @@ __global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
       // the previous P.V is done: P's buffer is free and O may be rescaled
       if (j > 0 && !mbar_wait(bar(L::bPVDone), (j - 1) & 1, a.status)) {
         failed = true;
+        drain_from = j + 1;
         break;
       }
       tc_fence_after();
@@ -464,6 +471,8 @@ __global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bPFull));
     }
+
+    for (int j = drain_from; j < nb; ++j) bar_sync_named(gbar, 128);
 
     // ---- epilogue: l = sum of every thread's partial sums (warp butterfly,
     // then the group's 4 warps in order), o = O^T / l, lse = (m + log2 l) ln 2
