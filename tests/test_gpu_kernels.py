@@ -60,6 +60,9 @@ DECODE_CASES = [
     (16, 8, 128, 4, [999, 4100]),
     (64, 8, 128, 1, [2500, 10]),
     (8, 8, 128, 1, [3000, 5, 2049]),
+    # q heads not a multiple of 4: the merge's register path (6 and 2 heads)
+    (6, 3, 128, 1, [5000, 2049, 7]),
+    (2, 1, 64, 16, [4100, 300]),
     (4, 1, 64, 1, [3000, 64]),
     # the larger pages the header allows
     (32, 8, 128, 32, [5000, 33, 1]),
@@ -142,6 +145,8 @@ PREFILL_CASES = [
     (32, 8, 128, 32, [(0, 500), (100, 40)], True, 0),
     (32, 8, 128, 64, [(4000, 300), (0, 65)], True, 0),
     (32, 8, 128, 256, [(0, 700), (300, 33)], True, 1024),
+    # q heads not a multiple of 4, several splits: the merge's register path
+    (6, 3, 128, 1, [(0, 700), (300, 70)], True, 256),
     (16, 8, 256, 64, [(0, 400), (70, 129)], True, 0),
     (8, 8, 64, 128, [(5, 250)], False, 0),
 ]
