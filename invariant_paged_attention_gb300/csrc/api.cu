@@ -742,6 +742,13 @@ namespace {
 // decode (qo_host == nullptr, one query per request) or a causal extend of
 // one-token q tiles (qo_host given), with one shared 512 + 64 wide latent
 // "kv head".
+// Tokens per q tile of an MLA call: an extend with 8 or 16 heads takes 32/Hq
+// consecutive tokens per CTA (their heads fill the kernel's 32 columns and
+// share each key block); a decode, or more heads, one token.
+int mla_tile_tokens(int num_heads, bool extend) {
+  return extend && num_heads < 32 && 32 % num_heads == 0 ? 32 / num_heads : 1;
+}
+
 int mla_plan(const bia_mla_desc *d, const int32_t *qo_host, const int32_t *kvp_host,
              const int32_t *last_host, int32_t batch, int32_t split, HostPlan *hp) {
   if (!d || d->page_size <= 0) return BIA_ERR_INVALID_ARG;
@@ -749,7 +756,8 @@ int mla_plan(const bia_mla_desc *d, const int32_t *qo_host, const int32_t *kvp_h
   if (!is_pow2(d->page_size) || d->page_size > 256) return BIA_ERR_UNSUPPORTED;
   if (!std::isfinite(d->sm_scale)) return BIA_ERR_INVALID_ARG;
   const bia_attn_desc as_attn{d->num_heads, 1, BIA_MLA_CKV_DIM, d->page_size, d->sm_scale};
-  return host_plan(&as_attn, qo_host, kvp_host, last_host, batch, 1, split, 1, 1, 1, 0, hp);
+  return host_plan(&as_attn, qo_host, kvp_host, last_host, batch, 1, split,
+                   mla_tile_tokens(d->num_heads, qo_host != nullptr), 1, 1, 0, hp);
 }
 
 size_t mla_workspace_size(const bia_mla_desc *desc, const int32_t *qo_host,
@@ -812,7 +820,8 @@ int run_mla(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
   pa.kv_last_page_len = kv_last_page_len;
   pa.batch = batch;
   pa.page_size = desc->page_size;
-  pa.tile_tokens = 1;
+  const int mla_tt = mla_tile_tokens(desc->num_heads, extend);
+  pa.tile_tokens = mla_tt;
   pa.tiles_per_unit = 1;
   pa.ctas = 1;
   pa.causal = 1;
@@ -848,7 +857,7 @@ int run_mla(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
   a.page_shift = log2i(desc->page_size);
   a.causal = 1;
   a.split = split_size;
-  a.tile_tokens = 1;
+  a.tile_tokens = mla_tt;
   const float sc = desc->sm_scale > 0.f
                        ? desc->sm_scale
                        : 1.0f / std::sqrt(static_cast<float>(BIA_MLA_CKV_DIM + BIA_MLA_KPE_DIM));
@@ -865,7 +874,7 @@ int run_mla(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
   a.status = pa.status;
   a.q_rows = static_cast<int32_t>(q_rows);
   a.kv_rows = static_cast<int32_t>(kv_rows);
-  const int hg = bia::mla_head_group(desc->num_heads);
+  const int hg = mla_tt > 1 ? 32 : bia::mla_head_group(desc->num_heads);
   int ce = encode_2d_map(&a.tm_q, q_nope, q_rows, BIA_MLA_CKV_DIM, hg);
   if (ce == 0) ce = encode_2d_map(&a.tm_qpe, q_pe, q_rows, BIA_MLA_KPE_DIM, hg);
   if (ce == 0) ce = encode_2d_map(&a.tm_k, ckv_cache, kv_rows, BIA_MLA_CKV_DIM, 1);

@@ -174,15 +174,22 @@ __global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
   if (u.b < 0) return;
   const ReqInfo r = a.reqs[u.b];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // u.tile: the query token's index within its request (0 for a decode
-  // query); causal, so token tq sees keys 0 .. kv_len - q_len + tq
-  const int32_t tq = u.tile;
-  const int32_t kv_end = r.kv_len - r.q_len + tq + 1;
+  // u.tile: the q tile of T = a.tile_tokens consecutive tokens of the
+  // request (T = 1: one token; a decode query is token 0).  With T > 1 (an
+  // extend with T x Hq = HG) the group's columns are the T tokens' heads,
+  // token-major, which are also consecutive rows of q and out.  Causal: token
+  // tq sees keys 0 .. kv_len - q_len + tq; the tile walks the keys of its
+  // last token, and each column stops at its own token's end.
+  const int T = a.tile_tokens;
+  const int32_t tq = u.tile * T;                   // the tile's first token
+  const int32_t t_last = min(tq + T, r.q_len) - 1; // its last token
+  const int32_t kv_end = r.kv_len - r.q_len + tq + 1; // keys of the first token
   const int64_t q_token = static_cast<int64_t>(r.q_start) + tq;
   const int32_t key_begin = u.split * a.split;
-  const int32_t key_end = min(key_begin + a.split, kv_end);
+  const int32_t key_end = min(key_begin + a.split, kv_end + (t_last - tq));
   const int nb = key_end > key_begin ? (key_end - key_begin + kKeys - 1) / kKeys : 0;
-  const int h_real = min(kHg, a.Hq - hg * kHg); // heads of this group (the rest are padding)
+  // columns of this group holding real (token, head) pairs (the rest are padding)
+  const int h_real = min(kHg, (t_last + 1 - tq) * a.Hq - hg * kHg);
 
   if (warp == kMmaWarpT) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (tid == 0) {
@@ -382,11 +389,14 @@ __global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
       uint32_t v[kHs];
       tmem_ld_n<kHs>(tS + h0 + lane_base, v);
       tmem_wait_ld();
-      const bool valid = key_begin + j * kKeys + t < key_end;
+      const int32_t key = key_begin + j * kKeys + t;
       float s[kHs];
 #pragma unroll
-      for (int h = 0; h < kHs; ++h)
-        s[h] = (valid && h0 + h < h_real) ? __uint_as_float(v[h]) * a.scale_log2 : -INFINITY;
+      for (int h = 0; h < kHs; ++h) {
+        // the column's token: tq + (h0 + h) / Hq when T > 1
+        const int32_t lim = T > 1 ? min(key_end, kv_end + (h0 + h) / a.Hq) : key_end;
+        s[h] = (key < lim && h0 + h < h_real) ? __uint_as_float(v[h]) * a.scale_log2 : -INFINITY;
+      }
       // P against the running max, computed while the block max is exchanged
       // (the running max rarely moves: then these are the final values)
       float p[kHs];
@@ -502,10 +512,17 @@ __global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
       const float lse = nz[h] ? __fmul_rn(__fadd_rn(m[h], lg2(ls)), kLn2) : -INFINITY;
       lse_mine = t == h ? lse : lse_mine;
     }
-    const bool single = (kv_end - 1) / a.split == 0; // one split: the final row
+    // one split for the whole tile: final rows (the merge folds a tile's rows
+    // whenever the tile spans several splits)
+    const bool single = (kv_end + (t_last - tq) - 1) / a.split == 0;
     const int64_t head0 = q_token * a.Hq + hg * kHg + h0;
-    const int64_t prow0 =
-        (r.rowbase + static_cast<int64_t>(tq) * r.nsp + u.split) * a.Hq + hg * kHg + h0;
+    // partial row of column h0 + h: its token's rows of this split
+    auto prow = [&](int h) {
+      const int c = hg * kHg + h0 + h;
+      const int tt = T > 1 ? c / a.Hq : 0;
+      return (r.rowbase + static_cast<int64_t>(tq + tt) * r.nsp + u.split) * a.Hq +
+             (T > 1 ? c % a.Hq : c);
+    };
 #pragma unroll
     for (int mb = 0; mb < kCkvPieces / 2; ++mb) {
       uint32_t o[kHs];
@@ -521,14 +538,14 @@ __global__ void __launch_bounds__(MlaCfg<HG>::kThreads, 1)
         if (single)
           a.out[(head0 + h) * kMlaCkvDim + d] = to_bf16(val);
         else
-          a.part_o[(prow0 + h) * kMlaCkvDim + d] = val;
+          a.part_o[prow(h) * kMlaCkvDim + d] = val;
       }
     }
     if (t < kHs && h0 + t < h_real) {
       if (single) {
         if (a.lse) a.lse[head0 + t] = lse_mine;
       } else {
-        a.part_lse[prow0 + t] = lse_mine;
+        a.part_lse[prow(t) + 0] = lse_mine;
       }
     }
   }
@@ -568,7 +585,8 @@ cudaError_t launch_mla_hg(const AttnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_mla_decode(const AttnArgs &a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
-  return mla_head_group(a.Hq) == 32 ? launch_mla_hg<32>(a, s) : launch_mla_hg<16>(a, s);
+  return a.tile_tokens > 1 || mla_head_group(a.Hq) == 32 ? launch_mla_hg<32>(a, s)
+                                                          : launch_mla_hg<16>(a, s);
 }
 
 } // namespace bia
