@@ -529,7 +529,8 @@ def sweep_mla(wl, bia, dev, stream, time_calls, emit):
     visible = sum(4 * kv - 6 for kv in ec.kv_lens)
     emit("MLA extend B=64 x 4 tokens, 16 heads, latent 512+64 (ctx U[1024,32768], page 1)",
          "prefill", visible * 16 * 2 * (576 + 512), cm, km,
-         {"latent_bytes_per_token_pass": visible * (512 + 64) * 2})
+         {"latent_bytes_per_token_pass": visible * (512 + 64) * 2,
+          "note": "16 heads: two tokens per CTA, so the rows are read once per pair"})
     del est, ec, ews, eout
     torch.cuda.empty_cache()
 
