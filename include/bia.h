@@ -332,16 +332,19 @@ BIA_API size_t bia_mla_decode_workspace_size(const bia_mla_desc *desc,
  *   q_nope [total_q, num_heads, 512] bf16, q_pe [total_q, num_heads, 64] bf16
  *   out    [total_q, num_heads, 512] bf16, lse [total_q, num_heads] fp32 or NULL
  *   split_size: keys per split-KV tile, a multiple of 128; 0 = BIA_PREFILL_SPLIT
- * Each q token runs as its own query against its own keys (the decode
- * kernel's fixed split tiles and ascending merge), so its bits depend only on
+ * Each q token is computed as its own query against its own keys (the decode
+ * kernel's fixed split tiles and ascending merge; with 8 or 16 heads, 32 /
+ * num_heads consecutive tokens share a CTA and each key block it reads, every
+ * token in its own MMA columns), so its bits depend only on
  * its request's keys up to its position and on split_size: the same in any
  * batch and under any chunking of the extend, on the q-tile grid or off it;
  * with equal split_size a token's bits equal those of bia_mla_decode_paged
  * for that position.  A request may have q_len = 0.  total_q * num_heads and
  * num_pages * page_size must stay below 2^31 (else BIA_ERR_UNSUPPORTED).
  * Arguments, ownership and errors otherwise as for bia_prefill_paged
- * (causal only).  The keys are read once per q token: this path suits short
- * extends (speculative tokens, small chunks), not long prompts.
+ * (causal only).  The keys are read once per q token (once per group of
+ * 32 / num_heads tokens with 8 or 16 heads): this path suits short extends
+ * (speculative tokens, small chunks), not long prompts.
  */
 BIA_API int bia_mla_prefill_paged(const bia_mla_desc *desc, const void *q_nope, const void *q_pe,
                           const void *ckv_cache, const void *kpe_cache, int64_t num_pages,
