@@ -742,8 +742,11 @@ def main():
 
     peaks, peak_kind = load_peaks()
     # counters are keyed by the kernel's own translation unit
-    pre_src = ["invariant_paged_attention_gb300/csrc/prefill.cu"]
-    dec_src = ["invariant_paged_attention_gb300/csrc/decode_tc.cu"]
+    pre_src = ["invariant_paged_attention_gb300/csrc/prefill.cu",
+               "invariant_paged_attention_gb300/csrc/softmax_rows.cuh",
+               "invariant_paged_attention_gb300/csrc/ptx.cuh"]
+    dec_src = ["invariant_paged_attention_gb300/csrc/decode_tc.cu",
+               "invariant_paged_attention_gb300/csrc/ptx.cuh"]
     roofline = roofline_of("tensor", flops, pk_avg * 1e3, peaks, peak_kind, "prefill_kernel<128>",
                            traffic_from_profiles("prefill_kernel<128>", pre_src, flops)) \
         if prefill else None

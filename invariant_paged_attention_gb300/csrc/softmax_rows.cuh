@@ -36,16 +36,16 @@ __device__ __forceinline__ float row_block_max(uint32_t taddr, int32_t n_vis,
 #pragma unroll
   for (int h = 0; h < KB / 64; ++h) {
     uint32_t v0[32], v1[32];
-    tmem_ld32(taddr + h * 64, v0);
-    tmem_ld32(taddr + h * 64 + 32, v1);
-    tmem_wait_ld();
-    if constexpr (MODE == kFull) {
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        bm = fmax3(bm, __uint_as_float(v0[i]), __uint_as_float(v0[i + 1]));
-        bm = fmax3(bm, __uint_as_float(v1[i]), __uint_as_float(v1[i + 1]));
-      }
+    if constexpr (MODE == kFull) { // every column counts: the load reduces them
+      float m0, m1;
+      tmem_ld32_max(taddr + h * 64, v0, m0);
+      tmem_ld32_max(taddr + h * 64 + 32, v1, m1);
+      tmem_wait_ld();
+      bm = fmax3(bm, m0, m1);
     } else {
+      tmem_ld32(taddr + h * 64, v0);
+      tmem_ld32(taddr + h * 64 + 32, v1);
+      tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         if (col_used<MODE>(h * 64 + i, n_vis, vis)) bm = fmaxf(bm, __uint_as_float(v0[i]));
