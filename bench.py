@@ -885,10 +885,21 @@ def main():
         pc, dc = wl.whole_prefill(pst), wl.whole_prefill(dst)
         f = prefill_call(pst, pc)
         cm, km, nl = leg.run([f], cs, cw)
-        put("cfg5_prefill_call", "tensor", prefill_flops(pc, 128, 32), cm, km, nl,
+        fl5, kb5 = prefill_flops(pc, 128, 32), kv_bytes(pc, 8, 128)
+        put("cfg5_prefill_call", "tensor", fl5, cm, km, nl,
             "prefill_kernel<128> + streamed tiles",
             "one 4096-token chunk (prefix 4096) + 64 one-token extends (ctx U[1024,32768]), "
-            "page 16", {"kv_bytes": kv_bytes(pc, 8, 128)})
+            "page 16", {"kv_bytes": kb5})
+        if km:
+            # the chunk's tiles are tensor-bound, the 64 extends stream their
+            # keys: the call's floor is both kernels at their own roofline,
+            # one after the other
+            floor = fl5 / (peaks["bf16_tflops"] * 1e9) + kb5 / (peaks["hbm_gbs"] * 1e6)
+            configs["cfg5_prefill_call"]["roofline_mixed"] = {
+                "bound": "tensor + hbm", "floor_ms": floor, "kernel_ms": km,
+                "frac": floor / km,
+                "note": "floor = flops / bf16 peak + kv bytes / HBM peak (of "
+                        f"{peak_kind}); frac = floor / the kernels' time"}
         f = decode_call(dst, dc)
         cm, km, nl = leg.run([f], cs, cw)
         put("cfg5_decodes", "hbm", kv_bytes(dc, 8, 128), cm, km, nl,
