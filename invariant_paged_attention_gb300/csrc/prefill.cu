@@ -373,10 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kPFull + t));
     }
-    // epilogue: o_s = O / l row by row into the tile's q buffer (free once
-    // its last MMA is done; rows of D*2 bytes), then copied out by whole rows
-    // so that every global store is coalesced.  bf16 rows for a tile with one
-    // split (one pass), else fp32 partial rows (two passes of D/2 columns).
+    // epilogue: o_s = O / l.  A tile with one split writes its bf16 rows
+    // straight from the thread that owns each row (16-byte stores); fp32
+    // partial rows go through the tile's q buffer (free once its last MMA is
+    // done; two passes of D/2 columns, rows of D*2 bytes) and are copied out
+    // by whole rows so that every global store is coalesced.
     if (me.has) {
       // warp-uniform (tcgen05.ld is warp-collective): a warp with a failed
       // wait writes zeros
@@ -404,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int pass_cols = final_row ? D : D / 2;
       const int n_pass = D / pass_cols;
       for (int ps = 0; ps < n_pass; ++ps) {
-        // this thread's row: chunk c at position c ^ (row % chunks); O read
-        // 32 columns at a time with the next load in flight
+        // this thread's row (fp32: chunk c staged at position c ^ (row %
+        // chunks)); O read 32 columns at a time with the next load in flight
         uint4 *my = reinterpret_cast<uint4 *>(stage + row * row_bytes);
         const int nchunk = pass_cols / 32;
         const uint32_t obase = tO(t) + lane_base + ps * pass_cols;
@@ -432,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
               w.y = pack_bf16(o[q * 8 + 2], o[q * 8 + 3]);
               w.z = pack_bf16(o[q * 8 + 4], o[q * 8 + 5]);
               w.w = pack_bf16(o[q * 8 + 6], o[q * 8 + 7]);
-              my[(c32 * 4 + q) ^ (row % chunks)] = w;
+              if (row_valid && c32 * 4 + q < Dr / 8)
+                reinterpret_cast<uint4 *>(a.out + out_row_of(row) * Dr)[c32 * 4 + q] = w;
             }
           } else {
 #pragma unroll
@@ -442,24 +444,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                              __float_as_uint(o[q * 4 + 2]), __float_as_uint(o[q * 4 + 3]));
           }
         }
+        if (final_row) continue; // one pass, written above
         bar_sync_named(1 + t, 128);
         // copy out: each warp takes 32 rows, chunks lanes per row
         const int tl = (warp & 3) * 32 + lane; // 0..127 within the tile's threads
         constexpr int rows_per_step = 128 / chunks; // rows the 128 threads cover per step
+        // 16-byte chunks of real columns (4 fp32 each)
+        const int c_lim = min(pass_cols, Dr - ps * pass_cols) / 4;
 #pragma unroll 4
         for (int r0 = 0; r0 < kTileRows; r0 += rows_per_step) {
           const int rr = r0 + tl / chunks, c = tl % chunks;
           const int32_t t_rr = me.tile * T + (rr >> gs);
-          // 16-byte chunks of real columns: 8 bf16 or 4 fp32 each
-          const int c_lim = final_row ? Dr / 8 : min(pass_cols, Dr - ps * pass_cols) / 4;
-          if (t_rr < r.q_len && c < c_lim) {
-            const uint4 w =
+          if (t_rr < r.q_len && c < c_lim)
+            reinterpret_cast<uint4 *>(a.part_o + part_row_of(rr) * Dr + ps * pass_cols)[c] =
                 reinterpret_cast<const uint4 *>(stage + rr * row_bytes)[c ^ (rr % chunks)];
-            if (final_row)
-              reinterpret_cast<uint4 *>(a.out + out_row_of(rr) * Dr)[c] = w;
-            else
-              reinterpret_cast<uint4 *>(a.part_o + part_row_of(rr) * Dr + ps * pass_cols)[c] = w;
-          }
         }
         bar_sync_named(1 + t, 128); // the stage is rewritten by the next pass
       }
