@@ -157,6 +157,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           tma_load_3d(sQ(t) + h * kAtom, &a.tm_q, 64 * h, kvh * G, r.q_start + ti[t].tile * T,
                       bar(L::kQFull));
   }
+  // This CTA gathers its 1/kCtas share of every block's rows for all CTAs of
+  // the cluster (producer lane = 4-row group x 64-column half); the first
+  // block's page indices load while the cluster handshake runs.
+  constexpr int kGroups = kKvBlock / kCtas / 4; // 4-row groups per CTA
+  const int rg = lane % kGroups, hh = lane / kGroups;
+  const int32_t row0 = (kKvBlock / kCtas) * static_cast<int32_t>(rank) + 4 * rg;
+  auto fetch = [&](int j, int32_t (&pg)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int32_t key = key_begin + j * kKvBlock + row0 + i;
+      pg[i] = (j < n_blocks && key < r.kv_len)
+                  ? __ldg(a.kv_indices + r.page_base + (key >> a.page_shift)) : -1;
+    }
+  };
+  int32_t pg[4] = {-1, -1, -1, -1};
+  if (warp == kProducerWarp) fetch(0, pg);
   tc_fence_before();
   cluster_sync(); // every CTA's barriers exist before any multicast reaches them
   tc_fence_after();
@@ -168,23 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     const int page_mask = (1 << a.page_shift) - 1;
-    // This CTA gathers its 1/kCtas share of every block's rows for all CTAs
-    // of the cluster: lane = 4-row group x 64-column half.
-    constexpr int kGroups = kKvBlock / kCtas / 4; // 4-row groups per CTA
-    const int rg = lane % kGroups, hh = lane / kGroups;
     const bool issues = hh < D / 64;
-    const int32_t row0 = (kKvBlock / kCtas) * static_cast<int32_t>(rank) + 4 * rg;
     const uint32_t dst_off = static_cast<uint32_t>(hh * kAtom + (row0 / 4) * 512);
-    auto fetch = [&](int j, int32_t (&pg)[4]) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int32_t key = key_begin + j * kKvBlock + row0 + i;
-        pg[i] = (j < n_blocks && key < r.kv_len)
-                    ? __ldg(a.kv_indices + r.page_base + (key >> a.page_shift)) : -1;
-      }
-    };
-    int32_t pg[4];
-    fetch(0, pg);
     for (int j = 0; j < n_blocks; ++j) {
       const int st = j & 1;
       int32_t rows[4];
