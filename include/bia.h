@@ -47,7 +47,15 @@
  * arrays are read synchronously during the call (to validate and to size the
  * launch) and must equal their device copies.  All work is enqueued on
  * `stream` (a cudaStream_t; NULL = legacy default stream) on the current
- * device.  A process drives one GPU: each kernel's shared-memory limit is
+ * device, with one exception that keeps the same ordering: a prefill call
+ * with both tensor-core q tiles and streamed single-token tiles runs the
+ * streamed tiles on a library-owned stream (one per host thread and device,
+ * created on first use and never destroyed) that waits for the call's plan
+ * on `stream`, and `stream` waits for it before the merge, so everything the
+ * call does comes after the work already on `stream` and before the work
+ * enqueued there next.  During a graph capture of `stream` the fork is
+ * captured with the call (if that thread's side stream does not exist yet,
+ * the call stays on `stream`).  A process drives one GPU: each kernel's shared-memory limit is
  * raised on its first launch, for the device current then, and a later
  * launch on another device fails with BIA_ERR_CUDA (one process per GPU is
  * the intended deployment).

@@ -17,6 +17,42 @@
 namespace {
 
 cudaEvent_t g_attn_begin = nullptr, g_attn_end = nullptr;
+
+// A library-owned stream (one per host thread and device) onto which a prefill
+// call forks its streamed single-token tiles, so that their key stream runs
+// beside the tensor-core tiles of the same call; the fork waits for the plan
+// and the call's stream waits for the fork before the merge, so the call is
+// ordered on the caller's stream exactly as without it.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+
+// The calling thread's side stream of the current device, created on first
+// use; nullptr when it cannot be had (then the call stays on one stream).
+// Nothing is created while `st` is being captured into a graph.
+SideStream *side_stream(cudaStream_t st) {
+  thread_local SideStream side[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream &s = side[dev];
+  if (s.stream) return &s;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return nullptr;
+  if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) {
+    s.stream = nullptr;
+    return nullptr;
+  }
+  if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaStreamDestroy(s.stream);
+    s.stream = nullptr;
+    return nullptr;
+  }
+  return &s;
+}
 unsigned long long g_launches = 0;
 thread_local char g_last_error[256] = "";
 
@@ -453,6 +489,16 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
     const cudaError_t re = cudaEventRecord(g_attn_begin, st);
     if (re != cudaSuccess) return cuda_fail("profile event record", re);
   }
+  // a prefill call with both kinds of tile forks its streamed single-token
+  // tiles onto the side stream (after the plan) and joins it before the merge
+  SideStream *side = !decode && hp.n_units > 0 && hp.n_sunits > 0 ? side_stream(st) : nullptr;
+  if (side && (cudaEventRecord(side->fork, st) != cudaSuccess ||
+               cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)) {
+    // a stale handle (the device was reset): forget it, stay on one stream
+    (void)cudaGetLastError();
+    *side = SideStream{};
+    side = nullptr;
+  }
   cudaError_t e = decode                     ? bia::launch_decode(a, st)
                   : desc->head_dim == 256 ? bia::launch_prefill_wide(a, st)
                                           : bia::launch_prefill(a, st);
@@ -462,9 +508,14 @@ int run_attention(bool decode, const bia_attn_desc *desc, const void *q, const v
     AttnArgs sa = a;
     sa.units = pa.sunits;
     sa.n_units = hp.n_sunits;
-    e = bia::launch_decode(sa, st);
+    e = bia::launch_decode(sa, side ? side->stream : st);
     if (e != cudaSuccess) return cuda_fail("streamed-tile kernel launch", e);
     __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+  }
+  if (side) {
+    cudaError_t je = cudaEventRecord(side->join, side->stream);
+    if (je == cudaSuccess) je = cudaStreamWaitEvent(st, side->join, 0);
+    if (je != cudaSuccess) return cuda_fail("side stream join", je);
   }
   if (profile) {
     const cudaError_t re = cudaEventRecord(g_attn_end, st);
