@@ -153,3 +153,39 @@ def test_captured_append_extend_and_mla_replay_bit_identically():
         assert same_bits(g[0], out) and same_bits(g[1], lse)
         assert same_bits(g[2], mout) and same_bits(g[3], mlse)
         assert torch.isfinite(g[0].float()).all() and torch.isfinite(g[2].float()).all()
+
+
+def test_capture_first_on_a_fresh_thread_matches_the_forked_eager_call():
+    """A prefill call with tensor-core tiles and a streamed one-token tile runs
+    the streamed tile on a per-thread side stream.  A thread whose first call
+    is being captured creates no side stream and keeps the call on one
+    stream; its replay gives the bits of the eager (forked) call."""
+    import threading
+    store = wl.PagedStore([wl.Sequence(8500 + i, p, n) for i, (p, n) in
+                           enumerate([(300, 97), (4000, 1), (0, 33)])], 32, 8, 128, 16, DEV,
+                          layout_seed=85)
+    call = wl.whole_prefill(store)
+    run = _setup(call, store, decode=False)
+    q = call.q.clone()
+    eager_out, eager_lse = [t.clone() for t in run(q)]  # this thread: forked
+    torch.cuda.synchronize()
+    result = {}
+
+    def capture_and_replay():
+        try:
+            torch.cuda.set_device(torch.device(DEV).index or 0)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                out, lse = run(q, stream=torch.cuda.current_stream())
+            graph.replay()
+            torch.cuda.synchronize()
+            result["out"], result["lse"] = out.clone(), lse.clone()
+        except Exception as e:  # reported on the test's thread
+            result["error"] = e
+
+    t = threading.Thread(target=capture_and_replay)
+    t.start()
+    t.join()
+    assert "error" not in result, result.get("error")
+    assert same_bits(result["out"], eager_out) and same_bits(result["lse"], eager_lse)
+    check_rows(call, result["out"], result["lse"])
