@@ -98,6 +98,9 @@ __host__ __device__ inline int32_t merge_first_token(int32_t q_len, int32_t kv_l
 // Slot of the workspace status array holding the number of rows to merge
 // (written by the planner; slot 0 is the status word).
 constexpr int kStatusMergeRows = 1;
+// Slot holding the work counter from which the persistent decode kernel's
+// CTAs take their next (unit, kv head) item (zeroed by the planner).
+constexpr int kStatusWorkCounter = 2;
 
 // A prefill request whose last q tile holds a single token (a one-token
 // extend, or the one-token tail of a longer chunk) has that tile streamed by

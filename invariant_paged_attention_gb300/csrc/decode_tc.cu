@@ -18,7 +18,12 @@
 // cache at several times that rate.
 //
 // The kernel is persistent: one CTA per SM takes the work items (unit, kv
-// head) round-robin, and its roles run ahead across items: the copy warps
+// head) from a counter (its first item is its own index; one copy thread
+// takes the next item while the copies of the current one are issued and
+// posts it to every role through a small mailbox in shared memory), so the
+// CTAs finish together whatever the mix of item sizes, and the items a
+// moment's CTAs work on stay neighbours (the kv heads of the same pages).
+// Its roles run ahead across items: the copy warps
 // stream the next item's q rows and key/value blocks while the MMAs finish
 // the current one, S and P are double-buffered (the next block's S is
 // computed while the softmax of this one runs), and O is double-buffered per
@@ -74,11 +79,13 @@ struct DecTcSmem {
   static constexpr int bKFull = 0, bKEmpty = bKFull + kKStagesT, bVFull = bKEmpty + kKStagesT,
                        bVEmpty = bVFull + kVStagesT, bQFull = bVEmpty + kVStagesT,
                        bQEmpty = bQFull + 2, bSFull = bQEmpty + 2, bPFull = bSFull + 2,
-                       bPVDone = bPFull + 2, bOFree = bPVDone + 2, kNumBars = bOFree + 2;
+                       bPVDone = bPFull + 2, bOFree = bPVDone + 2, bItemFull = bOFree + 2,
+                       bItemEmpty = bItemFull + 4, kNumBars = bItemEmpty + 4;
   static constexpr int kRed = kBar + 256;              // float [2][4 warps][16 heads]
   static constexpr int kLred = kRed + 2 * 4 * kNT * 4; // float [4 warps][16 heads]
   static constexpr int kSlot = kLred + 4 * kNT * 4;
-  static constexpr int kBytes = kSlot + 16;
+  static constexpr int kItems = kSlot + 16;            // int64 [4]: the item mailbox
+  static constexpr int kBytes = kItems + 4 * 8;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kKRing % 1024 == 0, "rings on the 128-byte swizzle period");
   static_assert(kP % 512 == 0 && kPBuf % 512 == 0, "P on the 64-byte swizzle period");
@@ -145,6 +152,7 @@ __global__ void __launch_bounds__((kProdWarpTc + tc_copy_warps(G)) * 32, 1)
     decode_tc_kernel(const __grid_constant__ AttnArgs a) {
   using L = DecTcSmem;
   constexpr int kProdThreadsT = tc_copy_warps(G) * 32;
+  constexpr int kReaderWarps = tc_copy_warps(G) + 1 + kSoftWarpsT; // copy, MMA, softmax
   constexpr int kKeyStepT = kProdThreadsT / 16; // keys between a copy thread's keys
   constexpr int kNkT = kKeysT / kKeyStepT;      // keys a copy thread takes per block
   constexpr int NL = G <= 8 ? 8 : 16; // TMEM columns a softmax thread loads
@@ -186,6 +194,10 @@ __global__ void __launch_bounds__((kProdWarpTc + tc_copy_warps(G)) * 32, 1)
       mbar_init(bar(L::bPVDone + i), 1);
       mbar_init(bar(L::bOFree + i), kSoftWarpsT);
     }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(L::bItemFull + i), 1);
+      mbar_init(bar(L::bItemEmpty + i), kReaderWarps); // every warp that reads items
+    }
     fence_mbar_init();
   }
   tc_fence_before();
@@ -196,6 +208,17 @@ __global__ void __launch_bounds__((kProdWarpTc + tc_copy_warps(G)) * 32, 1)
   // [32,48) and [48,64) (lanes = head-dim columns)
   auto tS = [&](uint32_t jg) { return tmem + 16u * (jg & 1u); };
   auto tO = [&](uint32_t ig) { return tmem + 32u + 16u * (ig & 1u); };
+  // the k-th item of this CTA, from mailbox slot k % 4 (-1: no more items, or
+  // a wait that ran out); read by a whole warp, or by one thread (single)
+  volatile int64_t *items = reinterpret_cast<volatile int64_t *>(smem + L::kItems);
+  auto read_item = [&](uint32_t k, bool single) -> int64_t {
+    const int s = static_cast<int>(k & 3u);
+    int64_t w = -1;
+    if (mbar_wait(bar(L::bItemFull + s), (k >> 2) & 1u, a.status)) w = items[s];
+    if (!single) __syncwarp();
+    if (single || lane == 0) mbar_arrive(bar(L::bItemEmpty + s));
+    return w;
+  };
 
   if (warp >= kProdWarpTc) {
     // ------------------------------------------------------------ copies
@@ -208,9 +231,38 @@ __global__ void __launch_bounds__((kProdWarpTc + tc_copy_warps(G)) * 32, 1)
     const uint32_t piece_off = static_cast<uint32_t>(cc >> 3) * kPieceT;
     uint32_t jg = 0, ig = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+    // copy thread 0 fetches the items: the first is the CTA's own index, each
+    // next one is taken from the counter when the current item starts and
+    // posted once the item's first block of copies is issued, so that the
+    // copy warps find it waiting when they reach it (one item ahead)
+    const bool fetcher = pt == 0;
+    if (fetcher) {
+      items[0] = blockIdx.x < n_work ? static_cast<int64_t>(blockIdx.x) : -1;
+      mbar_arrive(bar(L::bItemFull + 0));
+    }
+    int32_t taken = 0;   // the counter's answer for the next item
+    bool posted = false; // the next item is posted
+    auto post_next = [&](uint32_t k) { // item k + 1
+      if (!fetcher || posted) return;
+      posted = true;
+      int64_t nw = static_cast<int64_t>(gridDim.x) + taken;
+      if (nw >= n_work) nw = -1;
+      const uint32_t kn = k + 1;
+      if (kn >= 4 && !mbar_wait(bar(L::bItemEmpty + (kn & 3u)), ((kn >> 2) - 1) & 1u, a.status))
+        nw = -1;
+      items[kn & 3u] = nw;
+      mbar_arrive(bar(L::bItemFull + (kn & 3u)));
+    };
+    for (uint32_t k = 0; ok; ++k) {
+      const int64_t w = read_item(k, false);
+      if (w < 0) break;
+      if (fetcher) taken = atomicAdd(a.status + kStatusWorkCounter, 1);
+      posted = false;
       const TcItem it = tc_item(a, w);
-      if (!it.live) continue;
+      if (!it.live) {
+        post_next(k);
+        continue;
+      }
       // q rows of the item's G heads (rows G..15 zero) into q buffer ig % 2
       if (ig >= 2 && !mbar_wait(bar(L::bQEmpty + (ig & 1)), ((ig >> 1) - 1) & 1, a.status)) {
         ok = false;
@@ -294,7 +346,9 @@ __global__ void __launch_bounds__((kProdWarpTc + tc_copy_warps(G)) * 32, 1)
           cp_async_arrive(bar((kv == 0 ? L::bKFull : L::bVFull) + s));
         }
         if (!ok) break;
+        post_next(k); // after the first block
       }
+      post_next(k);
     }
     cp_async_wait_all(); // no copy outlives the CTA
   } else if (warp == kMmaWarpTc) {
@@ -319,7 +373,9 @@ __global__ void __launch_bounds__((kProdWarpTc + tc_copy_warps(G)) * 32, 1)
         mma_commit(bar(L::bKEmpty + s));
         mma_commit(bar(L::bSFull + (j_glob & 1)));
       };
-      for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      for (uint32_t k = 0; ok; ++k) {
+        const int64_t w = read_item(k, true);
+        if (w < 0) break;
         const TcItem it = tc_item(a, w);
         if (!it.live) continue;
         const uint32_t qb = qbuf(ig & 1);
@@ -371,7 +427,10 @@ __global__ void __launch_bounds__((kProdWarpTc + tc_copy_warps(G)) * 32, 1)
     float *lr = reinterpret_cast<float *>(smem + L::kLred);
     uint32_t jg = 0, ig = 0;
     bool failed = false; // the same on every softmax thread
-    for (int64_t w = blockIdx.x; w < n_work && !failed; w += gridDim.x) {
+    for (uint32_t k = 0; !failed; ++k) {
+      const int64_t w = read_item(k, false);
+      // the four warps share named barriers: they stop together
+      if (bar_any_named(1, 128, w < 0)) break;
       const TcItem it = tc_item(a, w);
       if (!it.live) continue;
       float m[G], l[G];

@@ -106,7 +106,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   // everything before it in the stream, since it rewrites the workspace.)
   grid_dep_launch();
   const int32_t gt = group_tiles(a.tiles_per_unit, a.ctas);
-  if (tid == 0) a.status[0] = 0;
+  if (tid == 0) {
+    a.status[0] = 0;
+    a.status[kStatusWorkCounter] = 0;
+  }
 
   // ---- A: per request
   const int per = (a.batch + kPlanThreads - 1) / kPlanThreads;
