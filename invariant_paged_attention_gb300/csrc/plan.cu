@@ -101,9 +101,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   __shared__ int64_t s_scan[kPlanThreads / 32];
   __shared__ int s_ok;
   const int tid = threadIdx.x;
-  // the attention kernel may start launching now: it waits for this plan
-  // before reading it.  (The planner itself is launched plainly, after
-  // everything before it in the stream, since it rewrites the workspace.)
+  // The planner rewrites the workspace: it waits for the kernel before it in
+  // the stream (it is launched chained, so only its launch overlaps that
+  // kernel), then lets the attention kernel start launching (which waits
+  // for this plan before reading it).
+  grid_dep_wait();
   grid_dep_launch();
   const int32_t gt = group_tiles(a.tiles_per_unit, a.ctas);
   if (tid == 0) {
@@ -255,8 +257,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 } // namespace
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {chained_launch_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, a);
 }
 
 } // namespace bia
